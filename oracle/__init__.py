@@ -1,0 +1,31 @@
+"""CPU oracle for the GroupQueryAttention forward pass.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package. The
+CUDA library under ``grouped_query_attention_gb300/`` never imports, links or
+calls anything here, and this package imports nothing from it.
+
+The oracle is the plain definition of the operator written out in numpy with
+fp64 arithmetic: no blocking, no online softmax, no split of the key axis.
+Every function cites the passage of the operator's documentation page it
+follows ("com.microsoft.GroupQueryAttention" README, sections Description,
+Inputs, Outputs, Attributes, Type constraints, Implementation variants).
+
+Pins: every function is checked in ``tests/test_oracle_pins.py`` against
+closed forms, invariants, a pure-Python brute force and a library routine
+(``torch.nn.functional.scaled_dot_product_attention`` in fp64). Readings that
+the pages leave open (query-head to KV-head mapping, window bound, order of
+softcap and bias, int8 rounding) are fixed by explicit switches whose default
+is the documented reading; those readings are "parity unpinned" by the pages
+themselves and are listed as such in the design notes.
+"""
+
+from .gqa import (  # noqa: F401
+    DEFAULT_ATTRS,
+    dequantize_int8,
+    gqa_forward,
+    quantize_int8,
+    rms_norm,
+    rotary_neox,
+    softcap_scores,
+)

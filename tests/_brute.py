@@ -1,0 +1,146 @@
+"""Pure-Python scalar brute force of the GroupQueryAttention forward pass.
+
+A second, independently written formulation used only to pin the numpy
+oracle on tiny shapes: scalar loops over every index, rotary as a complex
+multiplication, RMS norm and every sum through ``math.fsum``, the softmax as
+exp(s - logsumexp) with the sink logit inside the log-sum-exp. It shares no
+code with ``oracle/``.
+"""
+
+import math
+
+import numpy as np
+
+
+def _f(x):
+    return float(x)
+
+
+def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
+    N = attrs["num_heads"]
+    Nkv = attrs["kv_num_heads"]
+    q = inputs["query"]
+    k = inputs["key"]
+    v = inputs["value"]
+    B, S, hq = q.shape
+    H = hq // N
+    G = N // Nkv
+    half = H // 2
+    has_past = inputs.get("past_key") is not None
+    if share_buffer:
+        pk = [[[r.copy() for r in inputs["past_key"][b, g]] for g in range(Nkv)] for b in range(B)]
+        pv = [[[r.copy() for r in inputs["past_value"][b, g]] for g in range(Nkv)] for b in range(B)]
+        cache_dtype = inputs["past_key"].dtype
+    else:
+        pk = [[[r.copy() for r in present_key[b, g]] for g in range(Nkv)] for b in range(B)]
+        pv = [[[r.copy() for r in present_value[b, g]] for g in range(Nkv)] for b in range(B)]
+        cache_dtype = present_key.dtype
+    quant = attrs.get("k_quant_type", "NONE") != "NONE"
+    eps = attrs.get("qk_norm_epsilon", 1e-6)
+    qw = inputs.get("q_norm_weight")
+    kw = inputs.get("k_norm_weight")
+    rotary = attrs.get("do_rotary", 0) == 1
+    cosc = inputs.get("cos_cache")
+    sinc = inputs.get("sin_cache")
+    scale = attrs.get("scale", 0.0) or 1.0 / math.sqrt(H)
+    cap = attrs.get("softcap", 0.0)
+    W = attrs.get("local_window_size", -1)
+    causal = attrs.get("causal", 1) == 1
+    bias = inputs.get("attention_bias")
+    sink = inputs.get("head_sink")
+    smooth = attrs.get("smooth_softmax", -1) == 1
+
+    def norm(vec, w):
+        ms = math.fsum(x * x for x in vec) / len(vec)
+        r = 1.0 / math.sqrt(ms + eps)
+        return [vec[d] * r * _f(w[d]) for d in range(len(vec))]
+
+    def rope(vec, pos):
+        outv = list(vec)
+        for d in range(half):
+            z = complex(vec[d], vec[d + half]) * complex(_f(cosc[pos, d]), _f(sinc[pos, d]))
+            outv[d], outv[d + half] = z.real, z.imag
+        return outv
+
+    def scales(name, g):
+        sc = inputs[name].reshape(-1)
+        return [_f(sc[0]) if sc.size == 1 else _f(sc[g * H + d]) for d in range(H)]
+
+    def store(vec, g, name):
+        if quant:
+            sc = inputs[name].reshape(-1)
+            codes = []
+            for d in range(H):
+                s32 = sc[0] if sc.size == 1 else sc[g * H + d]
+                t = np.float32(vec[d]) / np.float32(s32)
+                codes.append(max(-127, min(127, round(float(t)))))   # Python round: ties to even
+            return np.array(codes, dtype=np.int8)
+        return np.array(vec, dtype=np.float64).astype(cache_dtype)
+
+    def value(row, g, name):
+        if quant:
+            sc = scales(name, g)
+            return [int(row[d]) * sc[d] for d in range(H)]
+        return [_f(x) for x in row]
+
+    out = np.zeros((B, S, N * H))
+    for b in range(B):
+        total = int(inputs["seqlens_k"][b]) + 1
+        past = total - S if has_past else 0
+        if has_past and not share_buffer:
+            for g in range(Nkv):
+                for j in range(past):
+                    pk[b][g][j] = inputs["past_key"][b, g, j].copy()
+                    pv[b][g][j] = inputs["past_value"][b, g, j].copy()
+        for g in range(Nkv):
+            for i in range(S):
+                kr = [_f(x) for x in k[b, i, g * H:(g + 1) * H]]
+                vr = [_f(x) for x in v[b, i, g * H:(g + 1) * H]]
+                if kw is not None:
+                    kr = norm(kr, kw)
+                if rotary:
+                    kr = rope(kr, past + i)
+                pk[b][g][past + i] = store(kr, g, "k_scale")
+                pv[b][g][past + i] = store(vr, g, "v_scale")
+        for h in range(N):
+            g = h // G
+            for i in range(S):
+                if not has_past and i >= total:
+                    continue
+                pos = past + i
+                qr = [_f(x) for x in q[b, i, h * H:(h + 1) * H]]
+                if qw is not None:
+                    qr = norm(qr, qw)
+                if rotary:
+                    qr = rope(qr, pos)
+                logits = []
+                for j in range(total):
+                    if causal and j > pos:
+                        continue
+                    if W >= 0 and j < pos - W:
+                        continue
+                    kj = value(pk[b][g][j], g, "k_scale")
+                    s = scale * math.fsum(qr[d] * kj[d] for d in range(H))
+                    if cap > 0:
+                        s = cap * math.tanh(s / cap)
+                    if bias is not None:
+                        bb = 0 if bias.shape[0] == 1 else b
+                        bh = 0 if bias.shape[1] == 1 else h
+                        s += _f(bias[bb, bh, i, j])
+                    logits.append((j, s))
+                sig = None
+                if sink is not None:
+                    sig = _f(sink[h])
+                elif smooth:
+                    sig = 0.0
+                allv = [s for _, s in logits] + ([sig] if sig is not None else [])
+                mx = max(allv)
+                lse = mx + math.log(math.fsum(math.exp(s - mx) for s in allv))
+                for d in range(H):
+                    terms = []
+                    for j, s in logits:
+                        terms.append(math.exp(s - lse) * value(pv[b][g][j], g, "v_scale")[d])
+                    out[b, i, h * H + d] = math.fsum(terms)
+    pk_arr = np.array([[np.stack(pk[b][g]) for g in range(Nkv)] for b in range(B)])
+    pv_arr = np.array([[np.stack(pv[b][g]) for g in range(Nkv)] for b in range(B)])
+    return out, pk_arr, pv_arr
