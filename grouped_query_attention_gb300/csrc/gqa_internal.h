@@ -1,0 +1,86 @@
+// Internal interface between the host entry points (gqa_api.cu) and the
+// kernel translation units. Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gqa {
+
+enum CacheMode : int { kPrompt = 0, kShared = 1, kCopy = 2 };
+enum ElemType : int { kF32 = 1, kF16 = 2, kI8 = 3 };
+
+// Everything a kernel needs about one gqa_forward call. Passed by value as a
+// kernel parameter (well under the 32 KB parameter limit).
+struct Params {
+  // ---- sizes
+  int B, S, N, Nkv, G, H;
+  int C;          // present capacity (sequence axis of present_key/value)
+  int past_cap;   // sequence axis of past_key/value (copy mode), else 0
+  int total_len;  // total_sequence_length (host scalar)
+  int mode;       // CacheMode
+  int t_type;     // ElemType of query/key/value/output (kF32 | kF16)
+  int cache_type; // ElemType of the cache (kF32 | kF16 | kI8)
+  int k_quant, v_quant;  // gqa_quant values
+  // ---- attributes (resolved)
+  int causal;
+  int window;            // local_window_size (-1 = none)
+  float scale;           // resolved score scale
+  float softcap;         // 0 = none
+  float eps;             // qk_norm_epsilon
+  int has_norm, has_rotary, has_bias, has_sink, smooth;
+  int bias_bdim, bias_ndim;  // leading dims of attention_bias (1 or B, 1 or N)
+  int bias_ld;               // last dim of attention_bias (total_sequence_length)
+  int rotary_rows;           // rows of cos/sin caches
+  int k_scale_n, v_scale_n;  // 1 or N_kv*H
+  // ---- tensors (device)
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* past_k;
+  const void* past_v;
+  void* present_k;
+  void* present_v;
+  const int* seqlens;
+  const void* cos_c;
+  const void* sin_c;
+  const void* bias;
+  const void* sink;
+  const float* k_scale;
+  const float* v_scale;
+  const void* qw;
+  const void* kw;
+  void* out;
+  // ---- workspace (device)
+  unsigned int* status;  // OR of GQA_DEVICE_* bits
+  void* qprep;           // prepared queries, layout [B][N_kv][S*G][H]
+  int qprep_type;        // ElemType of qprep
+  float* part_o;         // decode partial outputs [B*N_kv][max_splits][R][H]
+  float* part_ml;        // decode partial (m, l)   [B*N_kv][max_splits][R][2]
+  unsigned int* counters;  // decode merge tickets  [B*N_kv]
+  int split_len;         // keys per decode split
+  int max_splits;        // grid extent of the split axis
+  int rows_pad;          // R: decode rows per (b, g) rounded to a power of two
+};
+
+// Batch-level data check shared by all kernels: returns past_b (rows already
+// cached) or -1 if seqlens_k[b] is inconsistent with the shapes.
+__host__ __device__ inline int batch_past(const Params& p, int total) {
+  if (total < 1 || total > p.total_len || total > p.C) return -1;
+  if (p.mode == kPrompt) return total <= p.S ? 0 : -1;
+  int past = total - p.S;
+  if (past < 0) return -1;
+  if (p.mode == kCopy && past > p.past_cap) return -1;
+  return past;
+}
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_copy_past(const Params& p, cudaStream_t st);
+cudaError_t launch_prepass(const Params& p, cudaStream_t st);
+cudaError_t launch_decode(const Params& p, cudaStream_t st);
+cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st);
+bool decode_supported(const Params& p);
+bool prepass_supported(const Params& p);
+bool prefill_simt_supported(const Params& p);
+
+}  // namespace gqa

@@ -1,0 +1,232 @@
+// Pre-pass of the prefill path: appends the new K/V rows to the present cache
+// (RMS norm -> NeoX rotary -> cast or int8 code for K; cast or code for V) and
+// writes the prepared queries (norm -> rotary) to the workspace for the
+// attention kernel. One warp per row, 16-byte vector loads and stores.
+//
+// com.microsoft.GroupQueryAttention: section Inputs (q/k_norm_weight applied
+// before rotary; cos/sin_cache; k/v_scale), section Attributes
+// (qk_norm_epsilon, do_rotary, k/v_quant_type) and section Implementation
+// variants (new rows are appended at the live length before attention reads
+// the cache; copy mode keeps the live past rows).
+#include "common.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kMaxH = 256;
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int n = 4;
+};
+template <>
+struct Vec<__half> {
+  static constexpr int n = 8;
+};
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* src, float* dst);
+template <>
+__device__ __forceinline__ void load_vec<float>(const float* src, float* dst) {
+  float4 v = *reinterpret_cast<const float4*>(src);
+  dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_vec<__half>(const __half* src, float* dst) {
+  uint4 u = *reinterpret_cast<const uint4*>(src);
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 f = __half22float2(h[k]);
+    dst[2 * k] = f.x;
+    dst[2 * k + 1] = f.y;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec(T* dst, const float* src);
+template <>
+__device__ __forceinline__ void store_vec<float>(float* dst, const float* src) {
+  *reinterpret_cast<float4*>(dst) = make_float4(src[0], src[1], src[2], src[3]);
+}
+template <>
+__device__ __forceinline__ void store_vec<__half>(__half* dst, const float* src) {
+  uint4 u;
+  __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(src[2 * k], src[2 * k + 1]);
+  *reinterpret_cast<uint4*>(dst) = u;
+}
+
+// Row roles of the flattened row index.
+enum Role { kKey = 0, kValue = 1, kQuery = 2 };
+
+// T: element type of query/key/value. CacheT: element type of the cache
+// (T, or int8_t for a quantised cache). QT: element type of prepared queries.
+template <typename T, typename CacheT, typename QT>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+prepass_kernel(const Params p) {
+  __shared__ float rowbuf[kWarpsPerBlock][kMaxH];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long kv_rows = (long long)p.B * p.S * p.Nkv;
+  const long long q_rows = (long long)p.B * p.S * p.N;
+  const long long row = (long long)blockIdx.x * kWarpsPerBlock + warp;
+  if (row >= 2 * kv_rows + q_rows) return;
+
+  int role, b, i, head;
+  if (row < 2 * kv_rows) {
+    role = row < kv_rows ? kKey : kValue;
+    long long r = row - (role == kValue ? kv_rows : 0);
+    head = (int)(r % p.Nkv);
+    i = (int)((r / p.Nkv) % p.S);
+    b = (int)(r / ((long long)p.Nkv * p.S));
+  } else {
+    role = kQuery;
+    long long r = row - 2 * kv_rows;
+    head = (int)(r % p.N);
+    i = (int)((r / p.N) % p.S);
+    b = (int)(r / ((long long)p.N * p.S));
+  }
+  const int H = p.H;
+  const int total = p.seqlens[b] + 1;
+  const int past = batch_past(p, total);
+  if (past < 0) {
+    if (role == kKey && i == 0 && head == 0 && lane == 0) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
+    return;
+  }
+  const int pos = past + i;
+  const bool rotate = p.has_rotary && role != kValue;
+  if (rotate && pos >= p.rotary_rows) {
+    if (lane == 0) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
+    return;
+  }
+
+  constexpr int V = Vec<T>::n;
+  const T* src;
+  if (role == kQuery)
+    src = reinterpret_cast<const T*>(p.q) + ((long long)(b * p.S + i) * p.N + head) * H;
+  else
+    src = reinterpret_cast<const T*>(role == kKey ? p.k : p.v) + ((long long)(b * p.S + i) * p.Nkv + head) * H;
+
+  float* buf = rowbuf[warp];
+  float ss = 0.f;
+  for (int d0 = lane * V; d0 < H; d0 += 32 * V) {
+    float x[V];
+    load_vec<T>(src + d0, x);
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      buf[d0 + k] = x[k];
+      ss += x[k] * x[k];
+    }
+  }
+  const bool norm = p.has_norm && role != kValue;
+  float r = 1.f;
+  if (norm) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    r = 1.0f / sqrtf(ss / (float)H + p.eps);
+  }
+  __syncwarp();
+  const T* w = reinterpret_cast<const T*>(role == kQuery ? p.qw : p.kw);
+  const int half = H >> 1;
+  for (int d0 = lane * V; d0 < H; d0 += 32 * V) {
+    float y[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const int d = d0 + k;
+      float x = buf[d];
+      if (norm) x = (x * r) * load_t(w, d, p.t_type);
+      if (rotate) {
+        const int dp = d < half ? d + half : d - half;
+        float xp = buf[dp];
+        if (norm) xp = (xp * r) * load_t(w, dp, p.t_type);
+        const int dc = d < half ? d : d - half;
+        const float c = rot_t(p.cos_c, (long long)pos * half + dc, p.t_type);
+        const float s = rot_t(p.sin_c, (long long)pos * half + dc, p.t_type);
+        x = d < half ? (x * c - xp * s) : (x * c + xp * s);
+      }
+      y[k] = x;
+    }
+    if (role == kQuery) {
+      const int g = head / p.G, gi = head % p.G;
+      QT* dst = reinterpret_cast<QT*>(p.qprep) +
+                (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
+      store_vec<QT>(dst, y);
+    } else {
+      const long long off = (((long long)b * p.Nkv + head) * p.C + pos) * H + d0;
+      if constexpr (sizeof(CacheT) == 1) {
+        const float* sc = role == kKey ? p.k_scale : p.v_scale;
+        const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
+        char4 q4[V / 4];
+        int8_t* qb = reinterpret_cast<int8_t*>(q4);
+#pragma unroll
+        for (int k = 0; k < V; ++k) qb[k] = quant_i8(y[k], channel_scale(sc, nsc, head * H + d0 + k));
+        int8_t* dst = reinterpret_cast<int8_t*>(role == kKey ? p.present_k : p.present_v) + off;
+        if constexpr (V == 4) *reinterpret_cast<char4*>(dst) = q4[0];
+        else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
+      } else {
+        CacheT* dst = reinterpret_cast<CacheT*>(role == kKey ? p.present_k : p.present_v) + off;
+        store_vec<CacheT>(dst, y);
+      }
+    }
+  }
+}
+
+// Copy mode: present[b, g, 0:past_b] = past[b, g, 0:past_b] with 16-byte moves.
+__global__ void copy_past_kernel(const Params p, int esize) {
+  const int bg = blockIdx.y;
+  const int b = bg / p.Nkv, g = bg % p.Nkv;
+  const int total = p.seqlens[b] + 1;
+  const int past = batch_past(p, total);
+  if (past <= 0) return;
+  const long long row_bytes = (long long)p.H * esize;
+  const long long n16 = (long long)past * row_bytes / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      reinterpret_cast<const char*>(p.past_k) + ((long long)b * p.Nkv + g) * p.past_cap * row_bytes);
+  uint4* dst = reinterpret_cast<uint4*>(
+      reinterpret_cast<char*>(p.present_k) + ((long long)b * p.Nkv + g) * p.C * row_bytes);
+  const uint4* srcv = reinterpret_cast<const uint4*>(
+      reinterpret_cast<const char*>(p.past_v) + ((long long)b * p.Nkv + g) * p.past_cap * row_bytes);
+  uint4* dstv = reinterpret_cast<uint4*>(
+      reinterpret_cast<char*>(p.present_v) + ((long long)b * p.Nkv + g) * p.C * row_bytes);
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n16;
+       x += (long long)gridDim.x * blockDim.x) {
+    dst[x] = src[x];
+    dstv[x] = srcv[x];
+  }
+}
+
+}  // namespace
+
+bool prepass_supported(const Params& p) {
+  return p.H % 16 == 0 && p.H <= kMaxH && p.H >= 16;
+}
+
+cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.S * (2 * p.Nkv + p.N);
+  const unsigned blocks = (unsigned)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  if (blocks == 0) return cudaSuccess;
+  dim3 grid(blocks), block(kWarpsPerBlock * 32);
+  const bool q16 = p.qprep_type == kF16;
+  if (p.t_type == kF16) {
+    if (q16) prepass_kernel<__half, __half, __half><<<grid, block, 0, st>>>(p);
+    else prepass_kernel<__half, __half, float><<<grid, block, 0, st>>>(p);
+  } else if (p.cache_type == kI8) {
+    prepass_kernel<float, int8_t, float><<<grid, block, 0, st>>>(p);
+  } else {
+    prepass_kernel<float, float, float><<<grid, block, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_past(const Params& p, cudaStream_t st) {
+  const int esize = p.cache_type == kF32 ? 4 : (p.cache_type == kF16 ? 2 : 1);
+  dim3 grid(64, p.B * p.Nkv), block(256);
+  copy_past_kernel<<<grid, block, 0, st>>>(p, esize);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -155,6 +155,10 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
     sample: None for every output row, or an iterable of (b, h, i) triples;
       only those output rows are computed (the others stay 0). The caches
       are always updated in full.
+    Returns output (dtype of query), output_f64, present_key/value, and the
+    fp64 values of the appended rows before the storage cast
+    (appended_key_f64 / appended_value_f64, (B, N_kv, S, H)) with their
+    cache positions (appended_pos, (B, S)).
 
     com.microsoft.GroupQueryAttention: section Description (grouped-query
     attention over BSH Q/K/V and BNSH caches), sections Inputs / Outputs /
@@ -217,6 +221,9 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
             wanted.setdefault((int(b), int(h)), set()).add(int(i))
 
     out = np.zeros((B, S, N * H), dtype=np.float64)
+    new_k = np.zeros((B, Nkv, S, H))
+    new_v = np.zeros((B, Nkv, S, H))
+    new_pos = np.zeros((B, S), dtype=np.int64)
     for b in range(B):
         total_b = int(seqlens[b]) + 1
         past_b = total_b - S if has_past else 0
@@ -239,6 +246,8 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 kr = rotary_neox(kr, cos_c[pos], sin_c[pos])
             pk[b, g, pos] = _store(kr, pk.dtype, kq, k_scale, g, H)
             pv[b, g, pos] = _store(vr, pv.dtype, vq, v_scale, g, H)
+            new_k[b, g], new_v[b, g] = kr, vr
+        new_pos[b] = pos
 
         # Attention of every live query row over cache rows 0 .. total_b-1 as stored.
         live_rows = S if has_past else min(S, total_b)
@@ -287,4 +296,5 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
             den = e.sum(axis=1) + (np.exp(sigma - m_safe) if np.isfinite(sigma) else 0.0)
             o = (e @ vd) / np.where(ok, den, 1.0)[:, None]
             out[b, rows, h * H:(h + 1) * H] = np.where(ok[:, None], o, 0.0)
-    return dict(output=out.astype(out_dtype), output_f64=out, present_key=pk, present_value=pv)
+    return dict(output=out.astype(out_dtype), output_f64=out, present_key=pk, present_value=pv,
+                appended_key_f64=new_k, appended_value_f64=new_v, appended_pos=new_pos)

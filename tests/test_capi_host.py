@@ -1,0 +1,207 @@
+"""The C-ABI library on the host: it loads, exports every symbol include/gqa.h
+declares, and its host-side checks return the documented status codes.
+No CUDA call is made (gqa_create / gqa_workspace_size are host-only), so this
+runs without a GPU; device pointers are fake aligned addresses."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from grouped_query_attention_gb300 import capi
+from grouped_query_attention_gb300.inputs import WORKLOADS, CaseSpec
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    if not os.path.exists(capi.LIB_PATH):
+        from grouped_query_attention_gb300 import build
+        build.build()
+    return capi.load_library()
+
+
+def test_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "gqa.h")).read()
+    declared = set(re.findall(r"GQA_API\s+[\w\s\*]+?\b(gqa_\w+)\s*\(", header))
+    assert declared == set(capi.EXPORTS)
+    lib = ctypes.CDLL(capi.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for code, name in enumerate(["GQA_OK", "GQA_ERR_INVALID_ARGUMENT", "GQA_ERR_UNSUPPORTED", "GQA_ERR_CUDA",
+                                 "GQA_ERR_DEVICE_STATUS", "GQA_ERR_WORKSPACE"]):
+        assert capi.gqa_status_string(code) == name
+
+
+def test_attrs_defaults_match_page():
+    a = capi.gqa_attrs_default()
+    assert (a.causal, a.do_rotary, a.local_window_size, a.scale, a.softcap, a.smooth_softmax,
+            a.k_quant_type, a.v_quant_type, a.sliding_window_cache) == (1, 0, -1, 0.0, 0.0, -1, 0, 0, 0)
+    assert abs(a.qk_norm_epsilon - 1e-6) < 1e-12
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_heads=6, kv_num_heads=4), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=0, kv_num_heads=1), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=4, kv_num_heads=2, causal=0, local_window_size=8), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=4, kv_num_heads=2, local_window_size=-2), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=4, kv_num_heads=2, softcap=-1.0), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=4, kv_num_heads=2, k_quant_type=7), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=4, kv_num_heads=2, sliding_window_cache=1), capi.GQA_ERR_UNSUPPORTED),
+    (dict(num_heads=4, kv_num_heads=2, k_quant_type=2, v_quant_type=2, kv_cache_bit_width=4), capi.GQA_ERR_UNSUPPORTED),
+])
+def test_create_rejects(kw, status):
+    with pytest.raises(capi.GqaError) as e:
+        capi.gqa_create(capi.make_attrs(**kw))
+    assert e.value.status == status
+
+
+class FakeCall:
+    """Descriptors of a call with fake 256-byte-aligned device addresses."""
+
+    def __init__(self, dtype="f16", B=2, S=1, N=8, Nkv=2, H=128, C=64, mode="shared", **feat):
+        self.next = 0x10000
+        t = capi.GQA_F16 if dtype == "f16" else capi.GQA_F32
+        cache_t = capi.GQA_I8 if feat.get("quant") else t
+        self.inp = capi.GqaInputs()
+        self.out = capi.GqaOutputs()
+        self.inp.query = self.t(t, (B, S, N * H))
+        self.inp.key = self.t(t, (B, S, Nkv * H))
+        self.inp.value = self.t(t, (B, S, Nkv * H))
+        self.inp.seqlens_k = self.t(capi.GQA_I32, (B,))
+        self.inp.total_sequence_length = C if mode != "prompt" else S
+        self.out.output = self.t(t, (B, S, N * H))
+        self.out.present_key = self.t(cache_t, (B, Nkv, C, H))
+        self.out.present_value = self.t(cache_t, (B, Nkv, C, H))
+        if mode == "shared":
+            self.inp.past_key = self.out.present_key
+            self.inp.past_value = self.out.present_value
+        if feat.get("quant"):
+            n = 1 if feat["quant"] == "PER_TENSOR" else Nkv * H
+            self.inp.k_scale = self.t(capi.GQA_F32, (n,))
+            self.inp.v_scale = self.t(capi.GQA_F32, (n,))
+        self.attrs = dict(num_heads=N, kv_num_heads=Nkv)
+        if feat.get("quant"):
+            self.attrs.update(k_quant_type=feat["quant"], v_quant_type=feat["quant"])
+
+    def t(self, dtype, shape):
+        self.next += 1 << 24
+        return capi.describe(self.next, dtype, shape)
+
+    def size(self, **attr_over):
+        h = capi.gqa_create(capi.make_attrs(**{**self.attrs, **attr_over}))
+        try:
+            return capi.gqa_workspace_size(h, self.inp, self.out)
+        finally:
+            capi.gqa_destroy(h)
+
+
+def _expect(call, status, **attr_over):
+    with pytest.raises(capi.GqaError) as e:
+        call.size(**attr_over)
+    assert e.value.status == status, capi.gqa_last_error()
+
+
+def test_valid_calls_have_a_workspace():
+    for dtype in ("f16", "f32"):
+        for S in (1, 64):
+            assert FakeCall(dtype=dtype, S=S).size() > 0
+    assert FakeCall(dtype="f32", quant="PER_CHANNEL").size() > 0
+
+
+def test_workloads_validate():
+    for name, sp in WORKLOADS.items():
+        c = FakeCall(dtype=sp.dtype, B=sp.B, S=sp.S, N=sp.N, Nkv=sp.Nkv, H=sp.H, C=sp.capacity,
+                     mode=sp.mode, quant=sp.quant if sp.quant != "NONE" else None)
+        assert c.size() > 0, name
+
+
+def test_shape_and_dtype_errors():
+    c = FakeCall()
+    c.inp.key = c.t(capi.GQA_F16, (2, 1, 3 * 128))                       # wrong KV hidden size
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall()
+    c.inp.key = capi.GqaTensor()                                          # packed QKV
+    _expect(c, capi.GQA_ERR_UNSUPPORTED)
+    c = FakeCall()
+    c.inp.query = c.t(capi.GQA_BF16, (2, 1, 8 * 128))                     # bfloat16
+    _expect(c, capi.GQA_ERR_UNSUPPORTED)
+    c = FakeCall(dtype="f16", quant="PER_CHANNEL")                        # int8 cache needs fp32 Q/K/V
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall(dtype="f32", quant="PER_CHANNEL")
+    c.inp.k_scale = c.t(capi.GQA_F32, (7,))                               # scale length not 1 / N_kv*H
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall()
+    c.out.present_key = c.t(capi.GQA_F32, (2, 2, 64, 128))                # float cache of another dtype
+    c.out.present_value = c.t(capi.GQA_F32, (2, 2, 64, 128))
+    c.inp.past_key = capi.GqaTensor()
+    c.inp.past_value = capi.GqaTensor()
+    _expect(c, capi.GQA_ERR_UNSUPPORTED)
+    c = FakeCall(H=40, N=8)                                               # head size not a multiple of 16
+    _expect(c, capi.GQA_ERR_UNSUPPORTED)
+
+
+def test_cache_mode_errors():
+    c = FakeCall()
+    c.inp.past_value = c.t(capi.GQA_F16, (2, 2, 64, 128))                 # K shared, V not
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall(mode="copy")
+    c.inp.past_key = c.t(capi.GQA_F16, (2, 2, 60, 128))                   # present != past + S
+    c.inp.past_value = c.t(capi.GQA_F16, (2, 2, 60, 128))
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall(mode="prompt", S=8, C=4)                                 # capacity < S
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall()
+    _expect(c, capi.GQA_ERR_UNSUPPORTED, causal=0)                         # bidirectional with a past
+
+
+def test_optional_input_errors():
+    c = FakeCall()
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, do_rotary=1)                # rotary without cos/sin
+    c = FakeCall()
+    c.inp.cos_cache = c.t(capi.GQA_F16, (64, 32))                         # width != H/2
+    c.inp.sin_cache = c.t(capi.GQA_F16, (64, 32))
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, do_rotary=1)
+    c = FakeCall()
+    c.inp.q_norm_weight = c.t(capi.GQA_F16, (128,))                       # only one norm weight
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall()
+    c.inp.head_sink = c.t(capi.GQA_F16, (3,))                             # sink length != N
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall()
+    c.inp.attention_bias = c.t(capi.GQA_F16, (2, 3, 1, 64))               # head dim not 1 or N
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall()
+    c.inp.attention_bias = c.t(capi.GQA_F16, (1, 1, 1, 64))               # broadcast dims: fine
+    assert c.size() > 0
+
+
+def test_total_length_beyond_capacity_rejected():
+    c = FakeCall(C=64)
+    c.inp.total_sequence_length = 65
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+
+
+def test_plan_regimes():
+    h = capi.gqa_create(capi.make_attrs(num_heads=8, kv_num_heads=2))
+    try:
+        c = FakeCall(S=1)
+        info = capi.gqa_describe_plan(h, c.inp, c.out)
+        assert info.regime == capi.GQA_REGIME_DECODE and info.launches == 1 and info.split_len >= 64
+        c = FakeCall(S=64, C=128)
+        info = capi.gqa_describe_plan(h, c.inp, c.out)
+        assert info.regime == capi.GQA_REGIME_PREFILL and info.launches == 2
+        assert info.workspace_bytes == capi.gqa_workspace_size(h, c.inp, c.out)
+    finally:
+        capi.gqa_destroy(h)
+
+
+def test_misaligned_pointer_rejected():
+    c = FakeCall()
+    c.inp.query.data = c.inp.query.data + 2
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)

@@ -1,0 +1,101 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 oracle.
+
+Tiny sweeps cover every feature and cache mode, several splits / tiles and a
+ragged tail in both regimes (fused split-KV decode for S*G <= 8, pre-pass +
+flash prefill otherwise). The five workloads run at full size with the
+launch configuration the benchmark uses; their outputs are checked on
+sampled rows the oracle computes one by one and their caches in full.
+"""
+
+import numpy as np
+import pytest
+
+from grouped_query_attention_gb300.inputs import WORKLOADS, CaseSpec, generate
+from tests.parity import check_caches, check_output, run_gpu, run_oracle, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def spec(**kw):
+    base = dict(name="c", dtype="f16", B=3, S=1, N=8, Nkv=2, H=128, capacity=800, mode="shared",
+                seqlens_range=(100, 700))
+    base.update(kw)
+    return CaseSpec(**base)
+
+
+DECODE = {
+    "f16_h128_g4_rotary": spec(rotary_theta=1e4),
+    "f16_h64_g8_all_features": spec(H=64, N=16, Nkv=2, local_window_size=37, softcap=30.0, bias=(3, 16, 0.5),
+                                    head_sink=True, qk_norm=True, rotary_theta=1e4),
+    "f32_h128_g2_s2_smooth": spec(dtype="f32", N=4, Nkv=2, S=2, smooth_softmax=1, bias=(1, 4, 1.0)),
+    "i8_per_channel_h128_g4": spec(dtype="f32", quant="PER_CHANNEL"),
+    "i8_per_tensor_h64_s2_copy_norm_rotary": spec(dtype="f32", H=64, N=2, Nkv=2, S=2, mode="copy", past_len=600,
+                                                  seqlens_range=(50, 590), quant="PER_TENSOR", qk_norm=True,
+                                                  rotary_theta=1e4, scale_range=(0.02, 0.04)),
+    "f16_g8_copy": spec(N=8, Nkv=1, mode="copy", past_len=500, seqlens_range=(1, 500)),
+    "f16_prompt_s2_padding": spec(S=2, mode="prompt", capacity=4, seqlens_k=(0, 1, 1), seqlens_range=None,
+                                  rotary_theta=1e4),
+    "f32_g1_bias_shared": spec(dtype="f32", N=2, Nkv=2, bias=(1, 1, 0.5), seqlens_range=(0, 300)),
+    "f16_long_many_splits": spec(B=2, capacity=6000, seqlens_range=(3000, 5999)),
+    "f16_window_zero": spec(local_window_size=0),
+    "f32_bidirectional_prompt": spec(dtype="f32", mode="prompt", capacity=1, S=1, N=4, Nkv=1, causal=0,
+                                     seqlens_k=(0, 0, 0), seqlens_range=None),
+}
+
+PREFILL = {
+    "f32_prompt_tiny": WORKLOADS["prompt_f32_b1_s16"],
+    "f32_prompt_padding_h64_g4": spec(dtype="f32", H=64, N=8, Nkv=2, S=37, mode="prompt", capacity=40,
+                                      seqlens_k=(20, 36, 0), seqlens_range=None),
+    "f32_chunk_all_features": spec(dtype="f32", S=9, N=8, Nkv=2, local_window_size=50, softcap=20.0,
+                                   bias=(3, 8, 0.5), head_sink=True, qk_norm=True, rotary_theta=1e4),
+    "i8_per_channel_prefill": spec(dtype="f32", S=17, quant="PER_CHANNEL"),
+    "f16_h256_g2": spec(H=256, N=4, Nkv=2, S=20, capacity=500, seqlens_range=(20, 480)),
+    "f16_h128_g8_s65": spec(N=16, Nkv=2, S=65, seqlens_range=(65, 700), rotary_theta=1e4, qk_norm=True),
+    "f16_copy_s12": spec(S=12, N=8, Nkv=2, mode="copy", past_len=300, seqlens_range=(11, 311)),
+    "f32_bidirectional_prompt_s33": spec(dtype="f32", N=4, Nkv=2, S=33, mode="prompt", capacity=33, causal=0,
+                                         seqlens_k=(32, 20, 5), seqlens_range=None),
+    "f16_h32_smooth_window": spec(H=32, N=4, Nkv=1, S=24, local_window_size=5, smooth_softmax=1),
+}
+
+
+def _check(case, sample=None, repeat=1):
+    gpu = run_gpu(case, repeat=repeat)
+    assert gpu["status"] == 0, f"device status {gpu['status']:#x}"
+    ref = run_oracle(case, sample=sample)
+    check_output(case, gpu, ref, sample=sample)
+    check_caches(case, gpu, ref)
+    return gpu, ref
+
+
+@pytest.mark.parametrize("name", sorted(DECODE))
+def test_decode_parity(name):
+    _check(generate(DECODE[name], seed=21))
+
+
+@pytest.mark.parametrize("name", sorted(PREFILL))
+def test_prefill_parity(name):
+    _check(generate(PREFILL[name], seed=22))
+
+
+def test_decode_idempotent_repeat():
+    """Two calls in a row on a shared cache (the benchmark's loop) give the same result."""
+    case = generate(DECODE["f16_h128_g4_rotary"], seed=23)
+    _check(case, repeat=2)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_full_size(name):
+    case = generate(WORKLOADS[name], seed=0)
+    sample = None if name == "prompt_f32_b1_s16" else sample_rows(case, 48, seed=1)
+    _check(case, sample=sample)
+
+
+def test_bad_seqlens_sets_device_status():
+    """seqlens_k beyond the capacity: the batch entry is skipped and the status word says why."""
+    case = generate(DECODE["f16_h128_g4_rotary"], seed=24)
+    case["inputs"]["seqlens_k"] = case["inputs"]["seqlens_k"].copy()
+    case["inputs"]["seqlens_k"][1] = 10_000          # beyond total_sequence_length and the capacity (800)
+    gpu = run_gpu(case)
+    assert gpu["status"] & 1
+    # batch 1 is untouched
+    assert np.array_equal(gpu["present_key"][1], case["inputs"]["past_key"][1])
