@@ -46,19 +46,24 @@ __device__ __forceinline__ void load_vec<__half>(const __half* src, float* dst) 
   }
 }
 
-template <typename T>
-__device__ __forceinline__ void store_vec(T* dst, const float* src);
-template <>
-__device__ __forceinline__ void store_vec<float>(float* dst, const float* src) {
-  *reinterpret_cast<float4*>(dst) = make_float4(src[0], src[1], src[2], src[3]);
-}
-template <>
-__device__ __forceinline__ void store_vec<__half>(__half* dst, const float* src) {
-  uint4 u;
-  __half2* h = reinterpret_cast<__half2*>(&u);
+// Store V consecutive fp32 values as DstT (round to nearest), 16/8-byte stores.
+template <typename DstT, int V>
+__device__ __forceinline__ void store_n(DstT* dst, const float* src) {
+  static_assert(V % 4 == 0, "vector width");
+  if constexpr (sizeof(DstT) == 4) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(src[2 * k], src[2 * k + 1]);
-  *reinterpret_cast<uint4*>(dst) = u;
+    for (int k = 0; k < V; k += 4)
+      *reinterpret_cast<float4*>(dst + k) = make_float4(src[k], src[k + 1], src[k + 2], src[k + 3]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < V; k += 4) {
+      uint2 u;
+      __half2* h = reinterpret_cast<__half2*>(&u);
+      h[0] = __floats2half2_rn(src[k], src[k + 1]);
+      h[1] = __floats2half2_rn(src[k + 2], src[k + 3]);
+      *reinterpret_cast<uint2*>(dst + k) = u;
+    }
+  }
 }
 
 // Row roles of the flattened row index.
@@ -154,7 +159,7 @@ prepass_kernel(const Params p) {
       const int g = head / p.G, gi = head % p.G;
       QT* dst = reinterpret_cast<QT*>(p.qprep) +
                 (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
-      store_vec<QT>(dst, y);
+      store_n<QT, V>(dst, y);
     } else {
       const long long off = (((long long)b * p.Nkv + head) * p.C + pos) * H + d0;
       if constexpr (sizeof(CacheT) == 1) {
@@ -169,7 +174,7 @@ prepass_kernel(const Params p) {
         else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
       } else {
         CacheT* dst = reinterpret_cast<CacheT*>(role == kKey ? p.present_k : p.present_v) + off;
-        store_vec<CacheT>(dst, y);
+        store_n<CacheT, V>(dst, y);
       }
     }
   }
