@@ -3,9 +3,10 @@
 Tolerances: output |gpu - ref| <= atol + rtol * |ref| with (2e-3, 1e-2) for
 float16 and (1e-4, 1e-4) for float32 output, ref being the oracle's fp64
 value. Present caches: bit-exact, except appended K rows that went through
-RMS norm / rotary, whose stored value may be the neighbour of the oracle's
-rounding when the fp64 value lies within the fp32 compute error (8 ulp of
-the row's largest value) of a rounding midpoint (fp16), within 4 fp32 ulps
+RMS norm / rotary, whose stored value must be the fp16 rounding of a value
+within the fp32 compute error (8 fp32 ulps of the row's largest value) of the
+oracle's fp64 value (fp16; where rotary cancels a value into the fp16
+subnormal range that error spans more than one fp16 ulp), within 4 fp32 ulps
 of the row scale (fp32), or, for int8 codes, either integer when x/scale
 lies within 1e-3 of a half-integer.
 """
@@ -103,7 +104,7 @@ def _allowed_k_mismatch(case, ref, b, g, pos, gpu_row, ref_row):
         r = ref_row.astype(np.float64)
         eps32 = 8 * 2.0 ** -24 * np.abs(x).max()
         ulp = np.maximum(np.spacing(np.abs(gpu_row)).astype(np.float64), np.spacing(np.abs(ref_row)).astype(np.float64))
-        ok = (y == r) | ((np.abs(y - x) <= 0.5 * ulp + eps32) & (np.abs(y - r) <= ulp))
+        ok = (y == r) | (np.abs(y - x) <= 0.5 * ulp + eps32)
         return bool(ok.all())
     if gpu_row.dtype == np.float32:
         y = gpu_row.astype(np.float64)
@@ -135,8 +136,13 @@ def check_caches(case, gpu, ref):
             continue
         assert name == "present_key" and k_processed, f"{name}: {int(neq.sum())} rows differ"
         for (b, g, pos) in zip(*np.nonzero(neq)):
-            assert _allowed_k_mismatch(case, ref, b, g, pos, g_[b, g, pos], r_[b, g, pos]), \
-                f"{name}[{b},{g},{pos}] differs beyond the rounding rule"
+            if not _allowed_k_mismatch(case, ref, b, g, pos, g_[b, g, pos], r_[b, g, pos]):
+                gr, rr = g_[b, g, pos], r_[b, g, pos]
+                cols = np.nonzero(gr != rr)[0][:4]
+                s_idx = np.where(ref["appended_pos"][b] == pos)[0]
+                x = ref["appended_key_f64"][b, g, s_idx[0]][cols] if s_idx.size else None
+                raise AssertionError(f"{name}[{b},{g},{pos}] differs beyond the rounding rule: cols {cols}, "
+                                     f"gpu {gr[cols]}, oracle {rr[cols]}, fp64 {x}")
             tolerated += 1
     return tolerated
 
