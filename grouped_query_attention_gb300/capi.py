@@ -25,7 +25,7 @@ GQA_DEVICE_BAD_SEQLEN, GQA_DEVICE_BAD_ROTARY, GQA_DEVICE_TIMEOUT = 1, 2, 4
 
 EXPORTS = ["gqa_attrs_default", "gqa_create", "gqa_workspace_size", "gqa_forward",
            "gqa_read_device_status", "gqa_describe_plan", "gqa_destroy", "gqa_status_string",
-           "gqa_last_error"]
+           "gqa_last_error", "gqa_forward_noalloc"]
 GQA_REGIME_DECODE, GQA_REGIME_PREFILL = 1, 2
 
 
@@ -89,6 +89,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gqa_forward.argtypes = [ctypes.c_void_p, ctypes.POINTER(GqaInputs), ctypes.POINTER(GqaOutputs),
                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     lib.gqa_forward.restype = ctypes.c_int
+    lib.gqa_forward_noalloc.argtypes = [ctypes.c_void_p, ctypes.POINTER(GqaInputs), ctypes.POINTER(GqaOutputs),
+                                        ctypes.c_void_p]
+    lib.gqa_forward_noalloc.restype = ctypes.c_int
     lib.gqa_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.POINTER(ctypes.c_uint32)]
     lib.gqa_read_device_status.restype = ctypes.c_int
@@ -140,6 +143,12 @@ def gqa_forward(handle, inputs: GqaInputs, outputs: GqaOutputs, workspace: int, 
                 stream: int) -> None:
     _check(load_library().gqa_forward(handle, ctypes.byref(inputs), ctypes.byref(outputs),
                                       ctypes.c_void_p(workspace), workspace_bytes, ctypes.c_void_p(stream)))
+
+
+def gqa_forward_noalloc(handle, inputs: GqaInputs, outputs: GqaOutputs, stream: int) -> None:
+    """Decode-regime forward pass with the library's fixed scratch instead of a workspace."""
+    _check(load_library().gqa_forward_noalloc(handle, ctypes.byref(inputs), ctypes.byref(outputs),
+                                              ctypes.c_void_p(stream)))
 
 
 def gqa_read_device_status(handle, workspace: int, stream: int) -> int:

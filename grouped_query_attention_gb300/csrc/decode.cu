@@ -21,9 +21,18 @@
 // reduce-scatter over the 8 lanes leaves key (c >> 1)'s scores in lane c.
 // In the P.V phase every lane owns H/32 consecutive dims of all 16 keys of the
 // warp-iteration, with the probabilities broadcast through shared memory.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace gqa {
+
+// Fixed scratch for gqa_forward_noalloc: callers that cannot allocate device
+// memory get the decode kernel's status word, merge tickets and split
+// partials from this array instead of a workspace. Every GPU that loads the
+// library holds it until the process exits. Zero-initialised at load.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kWarps = 4;
@@ -528,6 +537,27 @@ cudaError_t launch_t(const Params& p, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t noalloc_scratch(void** ptr) {
+  // Device address of g_noalloc_scratch for the current device, looked up
+  // once per device (host code may not use the array's name as an address).
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = a;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 bool decode_supported(const Params& p) {
   return (p.H == 128 || p.H == 64) && p.S * p.G <= 8;

@@ -423,6 +423,33 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   return GQA_OK;
 }
 
+gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* out, void* stream) {
+  Plan pl;
+  gqa_status s = plan_call(h, in, out, &pl);
+  if (s != GQA_OK) return s;
+  if (!pl.decode)
+    return fail(GQA_ERR_UNSUPPORTED,
+                "gqa_forward_noalloc runs the decode regime only (S*num_heads/kv_num_heads <= 8, head size 64 or 128)");
+  if (pl.total_bytes > gqa::kNoAllocScratchBytes)
+    return fail(GQA_ERR_WORKSPACE, "call needs %zu bytes of scratch; the fixed scratch holds %zu (use gqa_forward)",
+                pl.total_bytes, gqa::kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  cudaError_t e = gqa::noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "address of the fixed scratch");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bind_workspace(&pl, scratch);
+  e = cudaMemsetAsync(scratch, 0, pl.hdr_bytes, st);  // status word and merge tickets start at zero
+  if (e != cudaSuccess) return cuda_fail(e, "scratch header clear");
+  const gqa::Params& P = pl.P;
+  if (P.mode == gqa::kCopy) {
+    e = gqa::launch_copy_past(P, st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
+  }
+  e = gqa::launch_decode(P, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return GQA_OK;
+}
+
 gqa_status gqa_read_device_status(gqa_handle* h, void* ws, void* stream, uint32_t* status) {
   if (!h || !ws || !status) return fail(GQA_ERR_INVALID_ARGUMENT, "NULL handle, workspace or status pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -74,6 +74,11 @@ __host__ __device__ inline int batch_past(const Params& p, int total) {
   return past;
 }
 
+// Size of the fixed scratch array behind gqa_forward_noalloc (16 MiB).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+// Device address of that array on the current device (looked up once per device).
+cudaError_t noalloc_scratch(void** ptr);
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_copy_past(const Params& p, cudaStream_t st);
 cudaError_t launch_prepass(const Params& p, cudaStream_t st);

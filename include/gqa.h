@@ -167,6 +167,31 @@ GQA_API gqa_status gqa_workspace_size(const gqa_handle* handle, const gqa_inputs
 GQA_API gqa_status gqa_forward(gqa_handle* handle, const gqa_inputs* in, const gqa_outputs* out,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Forward pass without any workspace, for callers that cannot allocate device
+ * memory: a plugin inside a host runtime that hands it only its input and output
+ * buffers and exposes no allocator, or code on a latency-critical path where
+ * cudaMalloc / cudaFree (which may synchronise the device) are not acceptable.
+ * The operator's pages have no counterpart: this is a deployment variant of
+ * gqa_forward's decode regime, with the same inputs, outputs and results.
+ *   - Scratch (status word, merge tickets, split partials) comes from one
+ *     fixed array of 16 MiB compiled into the library; every GPU that loads
+ *     the library holds it until the process exits. Nothing is allocated:
+ *     no cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Only the decode regime (S * num_heads / kv_num_heads <= 8, head size 64
+ *     or 128); other calls return GQA_ERR_UNSUPPORTED. A call that needs more
+ *     than 16 MiB of scratch returns GQA_ERR_WORKSPACE with the size it needs.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     each call clears the status word and tickets on its stream first. Calls
+ *     that overlap on the GPU (other streams, threads or handles) race and give
+ *     wrong results: serialise them.
+ *   - Data errors found on the device skip that batch entry as in gqa_forward,
+ *     but are not reported: no entry point reads this status word. */
+GQA_API gqa_status gqa_forward_noalloc(gqa_handle* handle, const gqa_inputs* in, const gqa_outputs* out,
+                                       void* stream);
+
 /* Synchronise `stream`, read and clear the status word that kernels of
  * earlier gqa_forward calls set in `workspace`. *status receives the OR of
  * GQA_DEVICE_* bits (0 = no data error). Returns DEVICE_STATUS if it is
