@@ -25,7 +25,8 @@ GQA_DEVICE_BAD_SEQLEN, GQA_DEVICE_BAD_ROTARY, GQA_DEVICE_TIMEOUT = 1, 2, 4
 
 EXPORTS = ["gqa_attrs_default", "gqa_create", "gqa_workspace_size", "gqa_forward",
            "gqa_read_device_status", "gqa_describe_plan", "gqa_destroy", "gqa_status_string",
-           "gqa_last_error", "gqa_forward_noalloc"]
+           "gqa_last_error", "gqa_forward_noalloc", "gqa_profile_begin", "gqa_profile_end"]
+KERNEL_KINDS = {1: "copy_past", 2: "prepass", 3: "decode", 4: "prefill_cuda_core", 5: "prefill_tensor_core"}
 GQA_REGIME_DECODE, GQA_REGIME_PREFILL = 1, 2
 
 
@@ -98,6 +99,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gqa_describe_plan.argtypes = [ctypes.c_void_p, ctypes.POINTER(GqaInputs), ctypes.POINTER(GqaOutputs),
                                       ctypes.POINTER(GqaPlanInfo)]
     lib.gqa_describe_plan.restype = ctypes.c_int
+    lib.gqa_profile_begin.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    lib.gqa_profile_begin.restype = ctypes.c_int
+    lib.gqa_profile_end.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_float),
+                                    ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    lib.gqa_profile_end.restype = ctypes.c_int
     lib.gqa_destroy.argtypes = [ctypes.c_void_p]
     lib.gqa_destroy.restype = None
     lib.gqa_status_string.argtypes = [ctypes.c_int]
@@ -165,6 +171,19 @@ def gqa_describe_plan(handle, inputs: GqaInputs, outputs: GqaOutputs) -> GqaPlan
     _check(load_library().gqa_describe_plan(handle, ctypes.byref(inputs), ctypes.byref(outputs),
                                             ctypes.byref(info)))
     return info
+
+
+def gqa_profile_begin(handle, max_launches: int) -> None:
+    _check(load_library().gqa_profile_begin(handle, int(max_launches)))
+
+
+def gqa_profile_end(handle, capacity: int = 4096) -> list:
+    """[(kernel kind name, milliseconds)] of the launches recorded since gqa_profile_begin."""
+    kinds = (ctypes.c_int32 * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = ctypes.c_int32()
+    _check(load_library().gqa_profile_end(handle, kinds, ms, capacity, ctypes.byref(n)))
+    return [(KERNEL_KINDS.get(kinds[i], str(kinds[i])), ms[i]) for i in range(min(n.value, capacity))]
 
 
 def gqa_destroy(handle) -> None:

@@ -14,6 +14,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "../../include/gqa.h"
 #include "gqa_internal.h"
@@ -22,6 +23,11 @@ struct gqa_handle {
   gqa_attrs attrs;
   void* zeroed_ws;          // workspace whose header (status + tickets) is known to be zero
   size_t zeroed_bytes;
+  // per-launch profiling (gqa_profile_begin / gqa_profile_end)
+  bool profiling;
+  std::vector<cudaEvent_t> events;  // 2 per launch
+  std::vector<int> kinds;
+  int used;
 };
 
 namespace {
@@ -75,6 +81,7 @@ std::string shape_str(const gqa_tensor& t) {
 struct Plan {
   gqa::Params P;
   bool decode;
+  bool tensor_core;  // prefill on the tcgen05 kernel (fp16, head size 128)
   size_t hdr_bytes, qprep_bytes, part_bytes, total_bytes;
 };
 
@@ -273,6 +280,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
 
   // ---- regime and workspace plan
   pl->decode = gqa::decode_supported(P);
+  pl->tensor_core = false;
   pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));
   pl->qprep_bytes = 0;
   pl->part_bytes = 0;
@@ -290,8 +298,9 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   } else {
     if (!gqa::prefill_simt_supported(P) || !gqa::prepass_supported(P))
       return fail(GQA_ERR_UNSUPPORTED, "no prefill kernel for head_size %lld", H);
-    P.qprep_type = gqa::kF32;
-    pl->qprep_bytes = align_up((size_t)B * S * N * H * sizeof(float));
+    pl->tensor_core = gqa::prefill_tc_supported(P);
+    P.qprep_type = pl->tensor_core ? gqa::kF16 : gqa::kF32;
+    pl->qprep_bytes = align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
   }
   pl->total_bytes = pl->hdr_bytes + pl->qprep_bytes + pl->part_bytes;
   return GQA_OK;
@@ -316,6 +325,19 @@ void bind_workspace(Plan* pl, void* ws) {
 
 gqa_status cuda_fail(cudaError_t e, const char* what) {
   return fail(GQA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Launch through `fn`, bracketed by an event pair when the handle is profiling.
+template <typename F>
+cudaError_t timed_launch(gqa_handle* h, int kind, cudaStream_t st, F fn) {
+  const bool rec = h->profiling && h->used < (int)h->kinds.size();
+  if (rec) cudaEventRecord(h->events[2 * h->used], st);
+  cudaError_t e = fn();
+  if (rec) {
+    cudaEventRecord(h->events[2 * h->used + 1], st);
+    h->kinds[h->used++] = kind;
+  }
+  return e;
 }
 
 }  // namespace
@@ -361,6 +383,8 @@ gqa_status gqa_create(const gqa_attrs* a, gqa_handle** out) {
   h->attrs = *a;
   h->zeroed_ws = nullptr;
   h->zeroed_bytes = 0;
+  h->profiling = false;
+  h->used = 0;
   *out = h;
   return GQA_OK;
 }
@@ -408,16 +432,19 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   const gqa::Params& P = pl.P;
   cudaError_t e;
   if (P.mode == gqa::kCopy) {
-    e = gqa::launch_copy_past(P, st);
+    e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
   if (pl.decode) {
-    e = gqa::launch_decode(P, st);
+    e = timed_launch(h, GQA_KERNEL_DECODE, st, [&] { return gqa::launch_decode(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   } else {
-    e = gqa::launch_prepass(P, st);
+    e = timed_launch(h, GQA_KERNEL_PREPASS, st, [&] { return gqa::launch_prepass(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "pre-pass launch");
-    e = gqa::launch_prefill_simt(P, st);
+    if (pl.tensor_core)
+      e = timed_launch(h, GQA_KERNEL_PREFILL_TENSOR_CORE, st, [&] { return gqa::launch_prefill_tc(P, st); });
+    else
+      e = timed_launch(h, GQA_KERNEL_PREFILL_CUDA_CORE, st, [&] { return gqa::launch_prefill_simt(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   }
   return GQA_OK;
@@ -442,10 +469,10 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
   if (e != cudaSuccess) return cuda_fail(e, "scratch header clear");
   const gqa::Params& P = pl.P;
   if (P.mode == gqa::kCopy) {
-    e = gqa::launch_copy_past(P, st);
+    e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
-  e = gqa::launch_decode(P, st);
+  e = timed_launch(h, GQA_KERNEL_DECODE, st, [&] { return gqa::launch_decode(P, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return GQA_OK;
 }
@@ -466,7 +493,55 @@ gqa_status gqa_read_device_status(gqa_handle* h, void* ws, void* stream, uint32_
   return GQA_OK;
 }
 
-void gqa_destroy(gqa_handle* h) { delete h; }
+gqa_status gqa_profile_begin(gqa_handle* h, int32_t max_launches) {
+  if (!h || max_launches < 1) return fail(GQA_ERR_INVALID_ARGUMENT, "NULL handle or max_launches < 1");
+  if (h->profiling) return fail(GQA_ERR_INVALID_ARGUMENT, "profiling already on");
+  h->events.assign(2 * (size_t)max_launches, nullptr);
+  for (auto& ev : h->events) {
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) {
+      for (auto& x : h->events)
+        if (x) cudaEventDestroy(x);
+      h->events.clear();
+      return cuda_fail(e, "event creation");
+    }
+  }
+  h->kinds.assign((size_t)max_launches, 0);
+  h->used = 0;
+  h->profiling = true;
+  return GQA_OK;
+}
+
+gqa_status gqa_profile_end(gqa_handle* h, int32_t* kinds, float* ms, int32_t capacity, int32_t* count) {
+  if (!h || !count || (capacity > 0 && (!kinds || !ms))) return fail(GQA_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (!h->profiling) return fail(GQA_ERR_INVALID_ARGUMENT, "profiling is not on");
+  gqa_status st = GQA_OK;
+  cudaError_t e = h->used > 0 ? cudaEventSynchronize(h->events[2 * h->used - 1]) : cudaSuccess;
+  if (e != cudaSuccess) st = cuda_fail(e, "event synchronize");
+  for (int i = 0; st == GQA_OK && i < h->used && i < capacity; ++i) {
+    float t = 0.f;
+    e = cudaEventElapsedTime(&t, h->events[2 * i], h->events[2 * i + 1]);
+    if (e != cudaSuccess) {
+      st = cuda_fail(e, "event elapsed time");
+      break;
+    }
+    kinds[i] = h->kinds[i];
+    ms[i] = t;
+  }
+  *count = h->used;
+  for (auto& ev : h->events) cudaEventDestroy(ev);
+  h->events.clear();
+  h->kinds.clear();
+  h->used = 0;
+  h->profiling = false;
+  return st;
+}
+
+void gqa_destroy(gqa_handle* h) {
+  if (!h) return;
+  for (auto& ev : h->events) cudaEventDestroy(ev);
+  delete h;
+}
 
 const char* gqa_status_string(gqa_status s) {
   switch (s) {

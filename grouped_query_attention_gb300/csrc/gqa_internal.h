@@ -84,6 +84,8 @@ cudaError_t launch_copy_past(const Params& p, cudaStream_t st);
 cudaError_t launch_prepass(const Params& p, cudaStream_t st);
 cudaError_t launch_decode(const Params& p, cudaStream_t st);
 cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st);
+cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st);
+bool prefill_tc_supported(const Params& p);
 bool decode_supported(const Params& p);
 bool prepass_supported(const Params& p);
 bool prefill_simt_supported(const Params& p);

@@ -1,0 +1,508 @@
+// Tensor-core flash prefill for GroupQueryAttention on sm_103a (fp16, head size 128).
+//
+// CTA = two 128-row query tiles of one KV head (b, g). Rows are the
+// (position, grouped head) pairs of that KV head, so every K/V tile the CTA
+// loads serves all G query heads of the group. Warp roles:
+//   warp 0       TMA: both query tiles once, then K and V tiles of 128 keys
+//                into a 2-stage ring (128-byte swizzle).
+//   warp 1       MMA issue (one thread): S_q = Q_q K^T into tensor memory,
+//                O_q += P_q V with P_q read from tensor memory; tensor-memory
+//                allocation; zeroes V rows past the key range (no NaN * 0).
+//   warps 2..5   softmax for query tile 0, warps 6..9 for query tile 1: one
+//                thread per row; scores from tensor memory, causal / window /
+//                live-length masks, softcap, bias, online max with lazy
+//                rescaling of O in tensor memory, P written back over S as
+//                fp16, epilogue O / l (+ sink term) to the output.
+// The two softmax groups ping-pong: while one works on its tile the tensor
+// core runs the other's MMAs. Tensor memory: S0 | S1 | O0 | O1 (512 columns).
+// Every barrier wait is bounded; on expiry the CTA sets the TIMEOUT status
+// bit, unwinds uniformly and still frees its tensor memory.
+//
+// com.microsoft.GroupQueryAttention, section Implementation variants
+// (qkv_present_flash_cluster, past_kv_flash_prefill and its rotary / softcap
+// / headsink / bias_headsink forms, share_append_split_flash_prefill:
+// clustered online-softmax prefill over the cache as stored, causal bound
+// right-aligned at the live length) and sections Inputs / Attributes.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "tcgen05.cuh"
+#include "tma_host.h"
+
+namespace gqa {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;                        // rows per query tile
+constexpr int kBN = 128;                        // keys per K/V tile
+constexpr int kHD = 128;                        // head size
+constexpr int kNS = 2;                          // K/V stages
+constexpr int kThreads = 320;                   // 10 warps
+constexpr uint32_t kBox = 128u * 128u;          // one 64-column box of 128 rows (fp16) = 16 KB
+constexpr uint32_t kTile = 2u * kBox;           // 128 rows x 128 columns = 32 KB
+constexpr float kLazy = 8.0f;                   // log2 growth tolerated before rescaling O
+constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);   // Q (K-major) x K (K-major)
+constexpr uint32_t kIdO = idesc_f16(128, 128, 0, 1);   // P (tensor memory) x V (MN-major)
+
+struct __align__(1024) TcSmem {
+  uint8_t q[2][kTile];
+  uint8_t k[kNS][kTile];
+  uint8_t v[kNS][kTile];
+  uint64_t q_full;
+  uint64_t k_full[kNS], v_full[kNS], kv_empty[kNS];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+};
+
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           bool accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// c * tanh(x / c) through exp2: tanh(u) = 1 - 2 / (exp(2u) + 1).
+__device__ __forceinline__ float softcap_apply(float x, float c, float inv_c) {
+  const float e = ex2(2.0f * kLog2e * x * inv_c);
+  return c * (1.0f - 2.0f * rcp_approx(e + 1.0f));
+}
+
+// Transformed score in the log2 domain: scale, softcap, + bias.
+__device__ __forceinline__ float score(float raw, float bias, float qk_scale, float cap, float inv_cap) {
+  float x = raw * qk_scale;
+  if (cap > 0.f) x = softcap_apply(x, cap, inv_cap) * kLog2e;
+  return x + bias * kLog2e;
+}
+
+// Bias values of keys j .. j+31 (columns col0 .. col0+31 of the tile); zeros
+// without a bias. 16-byte loads only where the address is 16-byte aligned and
+// the whole 8-key group is visible; otherwise per-key loads of visible keys
+// only (the bias row has total_sequence_length entries).
+__device__ __forceinline__ void load_bias32(const __half* row, int j, int col0, int lo, int hi, float* out) {
+  if (row == nullptr) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) out[e] = 0.f;
+    return;
+  }
+#pragma unroll
+  for (int g8 = 0; g8 < 32; g8 += 8) {
+    const __half* src = row + j + g8;
+    const int c0 = col0 + g8;
+    if (c0 >= lo && c0 + 8 <= hi && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h2[e]);
+        out[g8 + 2 * e] = f.x;
+        out[g8 + 2 * e + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) out[g8 + e] = (c0 + e >= lo && c0 + e < hi) ? __half2float(src[e]) : 0.f;
+    }
+  }
+}
+
+__device__ __forceinline__ bool aborted(const TcSmem& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
+}
+
+__device__ __forceinline__ void set_abort(const Params& p, TcSmem& sm) {
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+  flag_status(p, GQA_DEVICE_TIMEOUT_BIT);
+}
+
+// PLAIN: no softcap and no bias (the scores are the scaled products).
+template <bool PLAIN>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nrows = p.S * p.G;
+  const int nqb = (nrows + 2 * kBM - 1) / (2 * kBM);
+  const int qb = nqb - 1 - (int)blockIdx.x;  // longest key ranges first
+  const int bg = blockIdx.y, b = bg / p.Nkv, g = bg % p.Nkv;
+
+  // ---- block-uniform checks before any barrier or tensor memory
+  const int total = p.seqlens[b] + 1;
+  const int past = batch_past(p, total);
+  if (past < 0) {
+    if (qb == nqb - 1 && g == 0 && tid == 0) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
+    return;
+  }
+  if (p.has_rotary && past + p.S > p.rotary_rows) return;  // flagged by the pre-pass
+  const int live_i = p.mode == kPrompt ? min(p.S, total) : p.S;
+  const int r0 = qb * 2 * kBM;
+  const int i_lo = r0 / p.G;
+  const int i_hi = min((min(r0 + 2 * kBM, nrows) - 1) / p.G, live_i - 1);
+  if (i_lo > i_hi) {
+    // Only prompt padding rows here: their output is 0.
+    for (int x = tid; x < 2 * kBM * kHD; x += kThreads) {
+      const int r = r0 + x / kHD, d = x % kHD;
+      if (r >= nrows) continue;
+      const int i = r / p.G, h = g * p.G + r % p.G;
+      reinterpret_cast<__half*>(p.out)[((long long)(b * p.S + i) * p.N + h) * kHD + d] = __float2half_rn(0.f);
+    }
+    return;
+  }
+  const int kmax = p.causal ? min(total, past + i_hi + 1) : total;
+  // First key of the tile grid, rounded down to a multiple of 8 so that bias
+  // rows (when 16-byte aligned) are read with 16-byte loads; extra keys are masked.
+  const int kmin = (p.window >= 0 ? max(0, past + i_lo - p.window) : 0) & ~7;
+  const int ntiles = (kmax - kmin + kBN - 1) / kBN;
+
+  if (warp == 1) tmem_alloc(&sm.tmem, 512);
+  if (tid == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&sm.s_full[q], 1);
+      mbar_init(&sm.p_full[q], kBM);
+      mbar_init(&sm.o_done[q], 1);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  const int qrow0 = bg * nrows + r0;                 // row of Q0 in the prepared-query matrix
+  const int krow0 = bg * p.C + kmin;                 // row of the first key in the cache matrix
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      mbar_arrive_tx(&sm.q_full, 2 * kTile);
+      for (int q = 0; q < 2; ++q)
+        for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.q[q] + bx * kBox, &tmq, bx * 64, qrow0 + q * kBM, &sm.q_full);
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % kNS;
+        const uint32_t ph = (uint32_t)(t / kNS) & 1u;
+        if (!mbar_wait(&sm.kv_empty[st], ph ^ 1u) || aborted(sm)) {
+          set_abort(p, sm);
+          break;
+        }
+        const int row = krow0 + t * kBN;
+        mbar_arrive_tx(&sm.k_full[st], kTile);
+        for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.k[st] + bx * kBox, &tmk, bx * 64, row, &sm.k_full[st]);
+        mbar_arrive_tx(&sm.v_full[st], kTile);
+        for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.v[st] + bx * kBox, &tmv, bx * 64, row, &sm.v_full[st]);
+        issued = t + 1;
+      }
+      // Drain: no copy of this CTA may still be landing when it exits.
+      mbar_wait(&sm.q_full, 0);
+      for (int t = max(0, issued - kNS); t < issued; ++t) {
+        mbar_wait(&sm.k_full[t % kNS], (uint32_t)(t / kNS) & 1u);
+        mbar_wait(&sm.v_full[t % kNS], (uint32_t)(t / kNS) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    auto issue_s = [&](int q, int st) {
+      const uint32_t d = tmem + q * 128;
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (ks & 3) * 32;
+        mma_f16_ss(d, desc_kmajor_sw128(smem_addr(sm.q[q] + (ks >> 2) * kBox) + koff),
+                   desc_kmajor_sw128(smem_addr(sm.k[st] + (ks >> 2) * kBox) + koff), kIdS, ks > 0);
+      }
+      mma_commit(&sm.s_full[q]);
+    };
+    auto issue_pv = [&](int q, int st, bool acc) {
+      const uint32_t d = tmem + 256 + q * 128;
+      const uint32_t pa = tmem + q * 128;  // P over the first 64 columns of S_q
+      for (int ks = 0; ks < 8; ++ks)
+        mma_f16_ts(d, pa + ks * 8, desc_mnmajor_sw128(smem_addr(sm.v[st]) + ks * 2048, kBox, 1024), kIdO,
+                   acc || ks > 0);
+      mma_commit(&sm.o_done[q]);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.k_full[0], 0));
+    if (ok) {
+      if (lane == 0) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      __syncwarp();
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const int st = t % kNS;
+        const uint32_t ph = (uint32_t)(t / kNS) & 1u;
+        const uint32_t tp = (uint32_t)t & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph))) {
+          ok = false;
+          break;
+        }
+        // Zero V rows past the key range (stale cache rows may hold any bits).
+        const int valid = kmax - (kmin + t * kBN);
+        if (valid < kBN) {
+          for (int x = lane; x < (kBN - valid) * 16; x += 32) {
+            const int r = valid + x / 16, c = x % 16;
+            *reinterpret_cast<uint4*>(sm.v[st] + (c >> 3) * kBox + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        }
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[0], tp))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          issue_pv(0, st, t > 0);
+        }
+        __syncwarp();
+        const bool more = t + 1 < ntiles;
+        const int st1 = (t + 1) % kNS;
+        if (more && !__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st1], (uint32_t)((t + 1) / kNS) & 1u))) {
+          ok = false;
+          break;
+        }
+        if (more && lane == 0) issue_s(0, st1);
+        __syncwarp();
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[1], tp))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          issue_pv(1, st, t > 0);
+          mma_commit(&sm.kv_empty[st]);
+          if (more) issue_s(1, st1);
+        }
+        __syncwarp();
+        if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
+      }
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+    // Drain: every MMA this thread issued has finished before tensor memory is freed.
+    if (lane == 0) {
+      mma_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax groups
+    const int q = (warp - 2) >> 2;            // query tile of this group
+    const int quarter = warp & 3;             // tensor-memory lane quarter of this warp
+    const int rl = quarter * 32 + lane;       // row inside the tile
+    const int r = r0 + q * kBM + rl;          // row of the (b, g) block
+    const bool row_ok = r < nrows;
+    const int i = row_ok ? r / p.G : 0;
+    const int h = g * p.G + (row_ok ? r % p.G : 0);
+    const int pos = past + i;
+    const bool live = row_ok && i < live_i;
+    const int hi_key = live ? (p.causal ? min(total, pos + 1) : total) : 0;   // visible keys [lo_key, hi_key)
+    const int lo_key = p.window >= 0 ? max(0, pos - p.window) : 0;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + q * 128;
+    const uint32_t o_addr = tmem + lane_addr + 256 + q * 128;
+    const float qk_scale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
+    const float inv_cap = p.softcap > 0.f ? 1.0f / p.softcap : 0.f;
+    const __half* bias_row = nullptr;
+    if (p.has_bias && live)
+      bias_row = reinterpret_cast<const __half*>(p.bias) +
+                 (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
+                     p.bias_ld;
+    float m_run = kNegBig, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const bool got = mbar_wait(&sm.s_full[q], (uint32_t)t & 1u) && !aborted(sm);
+      if (!__all_sync(0xffffffffu, got)) {   // the warp leaves together
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int j0 = kmin + t * kBN;
+      const int lo = max(lo_key - j0, 0), hi = min(hi_key - j0, kBN);   // visible columns [lo, hi)
+      // Warp-uniform fast path: no row of this warp needs a mask on this tile.
+      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kBN);
+      // Pass 1: row max in the log2 domain. Plain scores: the whole row with
+      // four loads in flight and one wait, max of the raw products scaled once
+      // (the scale is positive). Softcap / bias: two halves of 64 columns,
+      // transformed in place and written back over S for pass 2.
+      float mt = kNegBig;
+      if constexpr (PLAIN) {
+        uint32_t r[kBN];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, r + c * 32);
+        tmem_ld_wait();
+        float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
+        if (full) {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(r[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kBN; ++e)
+            m4[e & 3] = (e >= lo && e < hi) ? fmaxf(m4[e & 3], __uint_as_float(r[e])) : m4[e & 3];
+        }
+        const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mt = m > kNegBig ? m * qk_scale : kNegBig;
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[64];
+          tmem_ld32(s_addr + hf * 64, r);
+          tmem_ld32(s_addr + hf * 64 + 32, r + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 64; c += 32) {
+            float bv[32];
+            load_bias32(bias_row, j0 + hf * 64 + c, hf * 64 + c, lo, hi, bv);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int col = hf * 64 + c + e;
+              const float x = score(__uint_as_float(r[c + e]), bv[e], qk_scale, p.softcap, inv_cap);
+              const float y = (full || (col >= lo && col < hi)) ? x : kNegBig;
+              mt = fmaxf(mt, y);
+              r[c + e] = __float_as_uint(y);
+            }
+          }
+          tmem_st32(s_addr + hf * 64, r);
+          tmem_st32(s_addr + hf * 64 + 32, r + 32);
+        }
+        tmem_st_wait();
+      }
+      // Lazy rescale: a row moves its reference max only when the tile max
+      // exceeds it by more than 2^8. The tensor-memory traffic is warp-wide,
+      // so the whole warp takes the branch and lanes that keep their max use f = 1.
+      const bool grow = mt > m_run + kLazy;
+      const float m_new = grow ? mt : m_run;
+      if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        // O_q is complete up to tile t-1 (its MMAs precede S_q(t)): rescale it in place.
+        const float f = grow ? ex2(m_run - m_new) : 1.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(o_addr + c * 32, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+          tmem_st32(o_addr + c * 32, raw);
+        }
+        l_run *= f;
+      }
+      m_run = m_new;
+      // Pass 2: P = exp2(score - m) as fp16 pairs over the first 64 columns of
+      // S_q, 64 scores per load batch; columns are overwritten only after read.
+      const float neg_m = -m_run;
+      float2 ls2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t r[64];
+        tmem_ld32(s_addr + hf * 64, r);
+        tmem_ld32(s_addr + hf * 64 + 32, r + 32);
+        tmem_ld_wait();
+        uint32_t packed[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int col = hf * 64 + 2 * k;
+          const float xa = __uint_as_float(r[2 * k]), xb = __uint_as_float(r[2 * k + 1]);
+          float pa, pb;
+          if constexpr (PLAIN) {
+            pa = ex2(fmaf(xa, qk_scale, neg_m));
+            pb = ex2(fmaf(xb, qk_scale, neg_m));
+            if (!full) {
+              pa = (col >= lo && col < hi) ? pa : 0.f;
+              pb = (col + 1 >= lo && col + 1 < hi) ? pb : 0.f;
+            }
+          } else {
+            pa = xa <= kNegBig ? 0.f : ex2(xa + neg_m);
+            pb = xb <= kNegBig ? 0.f : ex2(xb + neg_m);
+          }
+          ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
+          const __half2 hp = __floats2half2_rn(pa, pb);
+          packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        tmem_st32(s_addr + hf * 32, packed);
+      }
+      const float ls = ls2.x + ls2.y;
+      l_run += ls;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[q]);
+    }
+    // ---- epilogue: O / l (+ sink), fp16, one row per thread
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(ntiles - 1) & 1u) && !aborted(sm));
+    if (!ok) {
+      set_abort(p, sm);
+    } else {
+      tc_fence_after();
+      float mf = m_run, extra = 0.f;
+      if (p.has_sink || p.smooth) {
+        const float sg = (p.has_sink ? __half2float(reinterpret_cast<const __half*>(p.sink)[h]) : 0.f) * kLog2e;
+        mf = fmaxf(m_run, sg);
+        extra = ex2(sg - mf);
+      }
+      const float f = ex2(m_run - mf);
+      const float den = l_run * f + extra;
+      const float scale_out = (live && den > 0.f) ? f / den : 0.f;
+      __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)(b * p.S + i) * p.N + h) * kHD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t raw[32];
+        tmem_ld32(o_addr + c * 32, raw);   // all lanes (warp-wide); only real rows store
+        tmem_ld_wait();
+        if (!row_ok) continue;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 u;
+          __half2* h2 = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            h2[k] = __floats2half2_rn(__uint_as_float(raw[e + 2 * k]) * scale_out,
+                                      __uint_as_float(raw[e + 2 * k + 1]) * scale_out);
+          *reinterpret_cast<uint4*>(orow + c * 32 + e) = u;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const Params& p) {
+  return p.t_type == kF16 && p.cache_type == kF16 && p.H == kHD;
+}
+
+cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st) {
+  const long long qrows = (long long)p.B * p.Nkv * p.S * p.G;
+  const long long krows = (long long)p.B * p.Nkv * p.C;
+  CUtensorMap mq, mk, mv;
+  cudaError_t e = encode_fp16_2d_sw128(&mq, p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM);
+  if (e != cudaSuccess) return e;
+  if ((e = encode_fp16_2d_sw128(&mk, p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess) return e;
+  if ((e = encode_fp16_2d_sw128(&mv, p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess) return e;
+  const int smem = (int)sizeof(TcSmem) + 1024;
+  const bool plain = p.softcap <= 0.f && !p.has_bias;
+  auto kern = plain ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+  const int nrows = p.S * p.G;
+  dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
+  kern<<<grid, kThreads, smem, st>>>(p, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -1,0 +1,17 @@
+// Host-side encoding of TMA tensor maps (cuTensorMapEncodeTiled through the
+// runtime's driver entry point, so the library needs no link to libcuda).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gqa {
+
+// 2D map of a row-major [rows][cols] fp16 matrix with a 128-byte swizzle:
+// boxes of box_cols (<= 64) x box_rows elements. Returns a CUDA error code
+// (cudaErrorInvalidValue when the driver rejects the map).
+cudaError_t encode_fp16_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                                 uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+
+}  // namespace gqa

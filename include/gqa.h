@@ -218,6 +218,22 @@ typedef struct gqa_plan_info {
 GQA_API gqa_status gqa_describe_plan(const gqa_handle* handle, const gqa_inputs* in, const gqa_outputs* out,
                                      gqa_plan_info* info);
 
+/* Per-launch timing for measurement tools. gqa_profile_begin creates
+ * 2*max_launches CUDA events (host-side driver objects, no device memory);
+ * while profiling is on, every gqa_forward / gqa_forward_noalloc call on this
+ * handle records an event pair around each kernel it launches (up to
+ * max_launches launches in total). gqa_profile_end synchronises the events,
+ * writes up to `capacity` (kind, milliseconds) pairs in launch order, sets
+ * *count to the number of launches recorded, releases the events and turns
+ * profiling off. Kinds: */
+#define GQA_KERNEL_COPY_PAST 1
+#define GQA_KERNEL_PREPASS 2
+#define GQA_KERNEL_DECODE 3
+#define GQA_KERNEL_PREFILL_CUDA_CORE 4
+#define GQA_KERNEL_PREFILL_TENSOR_CORE 5
+GQA_API gqa_status gqa_profile_begin(gqa_handle* handle, int32_t max_launches);
+GQA_API gqa_status gqa_profile_end(gqa_handle* handle, int32_t* kinds, float* ms, int32_t capacity, int32_t* count);
+
 /* Release the handle (host memory only). NULL is a no-op. */
 GQA_API void gqa_destroy(gqa_handle* handle);
 

@@ -55,6 +55,15 @@ PREFILL = {
     "f32_bidirectional_prompt_s33": spec(dtype="f32", N=4, Nkv=2, S=33, mode="prompt", capacity=33, causal=0,
                                          seqlens_k=(32, 20, 5), seqlens_range=None),
     "f16_h32_smooth_window": spec(H=32, N=4, Nkv=1, S=24, local_window_size=5, smooth_softmax=1),
+    # tensor-core path (fp16, head size 128): ragged key tiles, query-tile tails, every feature
+    "f16_tc_all_features": spec(S=40, N=16, Nkv=2, local_window_size=100, softcap=30.0, bias=(3, 16, 0.5),
+                                head_sink=True, qk_norm=True, rotary_theta=1e4, seqlens_range=(40, 700)),
+    "f16_tc_prompt_padding_bias": spec(S=150, N=8, Nkv=2, mode="prompt", capacity=160, seqlens_k=(149, 70, 3),
+                                       seqlens_range=None, bias=(1, 1, 1.0)),
+    "f16_tc_bidirectional": spec(S=130, N=4, Nkv=2, mode="prompt", capacity=130, causal=0,
+                                 seqlens_k=(129, 100, 7), seqlens_range=None),
+    "f16_tc_smooth_multi_block": spec(B=2, S=300, N=8, Nkv=2, capacity=2500, seqlens_range=(300, 2400),
+                                      smooth_softmax=1, rotary_theta=1e4),
 }
 
 
