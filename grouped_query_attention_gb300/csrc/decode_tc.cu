@@ -1,0 +1,761 @@
+// Tensor-core split-KV decode for GroupQueryAttention on sm_103a (fp16 cache,
+// head size 128, at most 16 query rows per KV head).
+//
+// The R = S*G query rows of one KV head share every key, so each 128-key tile
+// is two small MMAs: S^T = K Q^T (M = 128 keys, N = 16 padded rows, K = 128
+// dims) and O^T += V^T P^T (M = 128 dims, V read as an MN-major operand,
+// N = 16, K = 128 keys). The CUDA cores only run the softmax (one thread per
+// key), so the kernel streams the cache at the memory rate.
+//
+// Work is balanced statically: the key range of every (batch b, KV head g)
+// is cut into 128-key tiles, the tiles of all (b, g) are laid end to end, and
+// persistent CTA c (one per SM) takes the c-th equal share of that sequence.
+// A share covers one or a few segments (the tiles of one (b, g) inside it);
+// only a share's first and last segment can be split with a neighbour CTA, so
+// a CTA writes at most two partial results. Warp roles:
+//   warp 2      preparer: maps the CTA's segments, prepares Q^T (norm, rotary,
+//               scale, fp16, 128-byte swizzle) in one of two item slots and
+//               appends the new rows that fall in the segment (then an
+//               async-proxy fence so TMA reads them); it runs one item ahead.
+//   warp 0      TMA: streams each published item's 128-key K and V tiles into
+//               a 3-stage ring.
+//   warp 1      MMA issue: S^T(t) into one of two tensor-memory buffers, then
+//               O^T += V^T P^T(t-1), so scores of the next tile are ready
+//               while the softmax works.
+//   warps 3..6  softmax: a thread holds one key's R scores (tensor-memory lane
+//               = key), masks / softcap / bias, cross-warp row max, lazy
+//               rescaling of O^T, P^T (fp16) into one of two shared buffers,
+//               zeroed V rows past the key range; at the end of an item one
+//               thread per dim writes the partial (or the output) and the last
+//               CTA to finish a shared (b, g) merges its partials (atomic
+//               ticket, no wait).
+// Every mbarrier wait is bounded; a timed-out consumer sets an abort flag that
+// all softmax warps check right after a shared named barrier, so they leave
+// together; tensor memory is always freed.
+//
+// com.microsoft.GroupQueryAttention, section Implementation variants
+// (share_append_split_decode_splitk / past_kv_decode_splitk: append, then
+// partition the key axis and merge partial online-softmax results) and
+// sections Inputs / Attributes.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "tcgen05.cuh"
+#include "tma_host.h"
+
+namespace gqa {
+namespace {
+
+using namespace tc;
+
+constexpr int kHD = 128;
+constexpr int kKT = kTcDecodeTile;       // keys per tile (128)
+constexpr int kNR = 16;                  // MMA N: query rows of the group, padded
+constexpr int kNS = 3;                   // K/V stages
+constexpr int kThreads = 224;            // TMA, MMA, preparer, 4 softmax warps
+constexpr int kSoftWarp0 = 3;            // first softmax warp
+constexpr int kSoft = 128;               // softmax threads
+constexpr uint32_t kBox = 128u * 128u;   // 64 columns x 128 rows (fp16) = 16 KB
+constexpr uint32_t kTile = 2u * kBox;    // K or V tile: 128 keys x 128 dims
+constexpr uint32_t kRowBox = 16u * 128u; // 64 columns x 16 rows = 2 KB
+constexpr float kLazy = 8.0f;            // log2 growth tolerated before rescaling O
+constexpr uint32_t kIdS = idesc_f16(128, kNR, 0, 0);   // K (K-major) x Q^T rows (K-major)
+constexpr uint32_t kIdO = idesc_f16(128, kNR, 1, 0);   // V (MN-major) x P^T rows (K-major)
+// Tensor memory: S^T buffers at columns 0 and 16, O^T at 32 (16 columns each).
+
+struct DItem {
+  int b, g;
+  int split, nsplit;     // this segment's index among the CTAs sharing (b, g), their count
+  int slot, slot0;       // partial slot of this segment / of the first segment of (b, g)
+  int cfirst;            // first CTA of (b, g)
+  int j0, jend;          // keys of this segment: [j0, jend)
+  int last;              // the segment holds the last tile of (b, g)
+  int past, total, ntiles, end;
+};
+
+struct __align__(1024) DSmem {
+  uint8_t k[kNS][kTile];
+  uint8_t v[kNS][kTile];
+  uint8_t qt[2][2 * kRowBox];   // per item slot: the group's query rows (16 x 128, fp16, swizzled)
+  uint8_t pt[2][2 * kRowBox];   // P^T buffers: 16 rows x 128 keys (fp16, swizzled)
+  float red[2][4][kNR];         // cross-warp row max, double-buffered by tile parity
+  float redl[4][kNR];           // cross-warp row sum
+  DItem item[2];
+  uint64_t full[kNS], empty[kNS];
+  uint64_t ifull[2], iempty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+  int last;
+};
+
+__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory"); }
+
+// Merge ticket with acquire-release ordering at GPU scope: after the named
+// barrier, the release covers every softmax thread's partial stores, and the
+// acquire makes the other splits' partials visible to the last one.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* addr) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(addr) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+__device__ __forceinline__ bool aborted(const DSmem& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
+}
+
+__device__ __forceinline__ void set_abort(const Params& p, DSmem& sm) {
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+  flag_status(p, GQA_DEVICE_TIMEOUT_BIT);
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Byte offset of element (row, col) in a [rows][128] fp16 matrix stored as two
+// 64-column boxes of `box` bytes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_elem(uint32_t row, uint32_t col, uint32_t box) {
+  return (col >> 6) * box + sw128_offset(row, (col & 63) >> 3) + (col & 7) * 2;
+}
+
+// ---------------------------------------------------------------- producer helpers
+
+// Tiles of batch b (its key range [kstart, total) in 128-key tiles, for each
+// KV head); 0 for a batch whose lengths are inconsistent.
+__device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, int& total, bool flag_bad) {
+  total = p.seqlens[b] + 1;
+  past = batch_past(p, total);
+  if (past >= 0 && p.has_rotary && past + p.S > p.rotary_rows) {
+    if (flag_bad) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
+    past = -1;
+  } else if (past < 0 && flag_bad) {
+    flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
+  }
+  if (past < 0) return 0;
+  const int kstart = p.window >= 0 ? max(0, past - p.window) : 0;
+  return (total - kstart + kKT - 1) / kKT;
+}
+
+// Number of tiles over all (b, g) (whole warp).
+__device__ long long count_tiles(const Params& p, bool flag_bad) {
+  const int lane = threadIdx.x & 31;
+  long long n = 0;
+  for (int b = lane; b < p.B; b += 32) {
+    int past, total;
+    n += (long long)batch_tiles(p, b, past, total, flag_bad) * p.Nkv;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  return n;
+}
+
+// CTA owning global tile t when `ntot` tiles are shared by `nc` <= ntot CTAs
+// (CTA c owns [c*ntot/nc, (c+1)*ntot/nc), never empty).
+__device__ __forceinline__ long long share_start(long long c, long long ntot, long long nc) { return c * ntot / nc; }
+__device__ __forceinline__ int tile_owner(long long t, long long ntot, long long nc) {
+  return (int)(((t + 1) * nc - 1) / ntot);
+}
+
+// The segment that starts at global tile t and ends at min(tend, end of its
+// (b, g)), with a warp-wide prefix scan of the per-batch tile counts.
+__device__ void map_segment(const Params& p, long long t, long long tend, long long ntot, long long nc,
+                            DItem& it) {
+  const int lane = threadIdx.x & 31;
+  long long base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    int past = -1, total = 0, tb = 0;
+    if (b < p.B) tb = batch_tiles(p, b, past, total, false);
+    const long long n = (long long)tb * p.Nkv;
+    long long incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long excl = base + incl - n;
+    const unsigned ballot = __ballot_sync(0xffffffffu, n > 0 && t >= excl && t < excl + n);
+    if (ballot) {
+      const int src = __ffs(ballot) - 1;
+      const int pp = __shfl_sync(0xffffffffu, past, src);
+      const int tt = __shfl_sync(0xffffffffu, total, src);
+      const int tiles = __shfl_sync(0xffffffffu, tb, src);
+      const long long r = t - __shfl_sync(0xffffffffu, excl, src);
+      it.b = __shfl_sync(0xffffffffu, b, src);
+      it.g = (int)(r / tiles);
+      const int lt = (int)(r % tiles);
+      const long long first = t - lt, bg_end = first + tiles;
+      const long long seg_end = tend < bg_end ? tend : bg_end;
+      const int kstart = p.window >= 0 ? max(0, pp - p.window) : 0;
+      it.past = pp;
+      it.total = tt;
+      it.j0 = kstart + lt * kKT;
+      it.jend = min(tt, kstart + (int)(seg_end - first) * kKT);
+      it.ntiles = (int)(seg_end - t);
+      it.last = seg_end == bg_end;
+      it.cfirst = tile_owner(first, ntot, nc);
+      it.nsplit = tile_owner(bg_end - 1, ntot, nc) - it.cfirst + 1;
+      it.split = (int)blockIdx.x - it.cfirst;
+      it.slot0 = 2 * it.cfirst + (share_start(it.cfirst, ntot, nc) != first ? 1 : 0);
+      it.slot = it.split == 0 ? it.slot0 : 2 * (int)blockIdx.x;
+      it.end = 0;
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  it.end = 1;   // not reached for t < ntot
+}
+
+// Row of H values held as x[e] = element lane + 32e: RMS norm then NeoX rotary
+// (the rotary partner of element e is e +- 2, in the same lane).
+__device__ __forceinline__ void norm_rope(const Params& p, float* x, const void* w, int pos, bool norm, bool rope) {
+  const int lane = threadIdx.x & 31;
+  if (norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ss += x[e] * x[e];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rn = 1.0f / sqrtf(ss / (float)kHD + p.eps);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = (x[e] * rn) * load_t(w, lane + 32 * e, p.t_type);
+  }
+  if (rope) {
+    float y[4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int dc = lane + 32 * e;
+      const float cs = load_t(p.cos_c, (long long)pos * (kHD / 2) + dc, p.t_type);
+      const float sn = load_t(p.sin_c, (long long)pos * (kHD / 2) + dc, p.t_type);
+      y[e] = x[e] * cs - x[e + 2] * sn;
+      y[e + 2] = x[e + 2] * cs + x[e] * sn;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = y[e];
+  }
+}
+
+// The group's query rows of an item as fp16 MMA operand rows (scaled into the
+// log2 domain unless softcap). Rows >= R stay zero from the kernel start.
+__device__ void prepare_qt(const Params& p, const DItem& it, uint8_t* qt) {
+  const int lane = threadIdx.x & 31;
+  const int rows = p.S * p.G;
+  const float qscale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
+  for (int r = 0; r < rows; ++r) {
+    const int i = r / p.G, h = it.g * p.G + r % p.G;
+    const long long src = ((long long)(it.b * p.S + i) * p.N + h) * kHD;
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = load_t(p.q, src + lane + 32 * e, p.t_type);
+    norm_rope(p, x, p.qw, it.past + i, p.has_norm, p.has_rotary);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<__half*>(qt + sw_elem(r, lane + 32 * e, kRowBox)) = __float2half_rn(x[e] * qscale);
+  }
+}
+
+// Append the new rows of (b, g) that fall in the segment's keys to the
+// present cache (K: norm, rotary; cast to fp16). Prompt padding rows (past the
+// total length) go with the segment that holds the last tile.
+__device__ void append_rows(const Params& p, const DItem& it) {
+  const int lane = threadIdx.x & 31;
+  for (int i = 0; i < p.S; ++i) {
+    const int j = it.past + i;
+    const bool mine = j < it.total ? (j >= it.j0 && j < it.jend) : it.last != 0;
+    if (!mine) continue;
+    const long long src = ((long long)(it.b * p.S + i) * p.Nkv + it.g) * kHD;
+    const long long dst = (((long long)it.b * p.Nkv + it.g) * p.C + j) * kHD;
+    float x[4], v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] = load_t(p.k, src + lane + 32 * e, p.t_type);
+      v[e] = load_t(p.v, src + lane + 32 * e, p.t_type);
+    }
+    norm_rope(p, x, p.kw, j, p.has_norm, p.has_rotary);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      reinterpret_cast<__half*>(p.present_k)[dst + lane + 32 * e] = __float2half_rn(x[e]);
+      reinterpret_cast<__half*>(p.present_v)[dst + lane + 32 * e] = __float2half_rn(v[e]);
+    }
+  }
+}
+
+// Output value of row r, dim d from (m, l, o): sink / smooth-softmax term, 1/l, fp16.
+__device__ __forceinline__ void write_out(const Params& p, int b, int g, int total, int r, int d, float m, float l,
+                                          float o) {
+  const int i = r / p.G, h = g * p.G + r % p.G;
+  const long long oi = ((long long)(b * p.S + i) * p.N + h) * kHD + d;
+  float val;
+  if (p.mode == kPrompt && i >= total) {
+    val = 0.f;
+  } else {
+    float mf = m, extra = 0.f;
+    if (p.has_sink || p.smooth) {
+      const float sg = (p.has_sink ? load_t(p.sink, h, p.t_type) : 0.f) * kLog2e;
+      mf = fmaxf(m, sg);
+      extra = ex2(sg - mf);
+    }
+    const float f = ex2(m - mf);
+    const float den = l * f + extra;
+    val = den > 0.f ? o * f / den : 0.f;
+  }
+  reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(val);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  DSmem& sm = *reinterpret_cast<DSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 1) tmem_alloc(&sm.tmem, 64);
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.ifull[s], 1);
+      mbar_init(&sm.iempty[s], 2);  // MMA commit (Q^T reads done) + softmax release
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.s_free[s], kSoft);
+      mbar_init(&sm.p_full[s], kSoft);
+      mbar_init(&sm.p_free[s], 1);
+    }
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    sm.last = 0;
+    mbar_fence_init();
+  }
+  // Query / probability rows >= R are zero for the whole kernel.
+  for (int x = tid; x < (int)(2 * 2 * kRowBox / 16); x += kThreads) {
+    reinterpret_cast<uint4*>(&sm.qt[0][0])[x] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(&sm.pt[0][0])[x] = make_uint4(0, 0, 0, 0);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+
+  if (warp == 2) {
+    // ================================================================ preparer
+    // With fewer tiles than CTAs only the first `ntot` CTAs work, so that
+    // every working CTA's share is non-empty and the CTAs sharing a (b, g)
+    // are consecutive.
+    const long long ntot = count_tiles(p, blockIdx.x == 0);
+    const long long nc = ntot < (long long)gridDim.x ? ntot : (long long)gridDim.x;
+    long long t = 0, tend = 0;
+    if ((long long)blockIdx.x < nc) {
+      t = share_start(blockIdx.x, ntot, nc);
+      tend = share_start(blockIdx.x + 1, ntot, nc);
+    }
+    int slot = 0;
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    while (true) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iempty[slot], iphase[slot] ^ 1u)) || aborted(sm)) {
+        ok = false;
+        break;
+      }
+      if (t >= tend) {
+        if (lane == 0) {
+          sm.item[slot].end = 1;
+          mbar_arrive(&sm.ifull[slot]);
+        }
+        break;
+      }
+      DItem it;
+      map_segment(p, t, tend, ntot, nc, it);
+      if (it.end) {   // unreachable: every t < ntot maps to a segment
+        ok = false;
+        break;
+      }
+      t += it.ntiles;
+      if (lane == 0) sm.item[slot] = it;
+      prepare_qt(p, it, sm.qt[slot]);
+      append_rows(p, it);
+      fence_async_all();  // query rows (shared) and appended rows (global) -> async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ifull[slot]);
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+  } else if (warp == 0) {
+    // ================================================================ TMA
+    int slot = 0, tau = 0;
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    while (ok) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.ifull[slot], iphase[slot]))) {
+        ok = false;
+        break;
+      }
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+      const int row0 = (it.b * p.Nkv + it.g) * p.C + it.j0;
+      for (int t = 0; t < it.ntiles; ++t, ++tau) {
+        const int st = tau % kNS;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.empty[st], ((uint32_t)(tau / kNS) & 1u) ^ 1u)) || aborted(sm)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_tx(&sm.full[st], 2 * kTile);
+          for (int bx = 0; bx < 2; ++bx) {
+            tma_load_2d(sm.k[st] + bx * kBox, &tmk, bx * 64, row0 + t * kKT, &sm.full[st]);
+            tma_load_2d(sm.v[st] + bx * kBox, &tmv, bx * 64, row0 + t * kKT, &sm.full[st]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+    // Drain: every tile this warp issued has landed before the CTA can exit.
+    for (int u = max(0, tau - kNS); u < tau; ++u) mbar_wait(&sm.full[u % kNS], (uint32_t)(u / kNS) & 1u);
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    int slot = 0, tau = 0;
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    auto issue_pv = [&](int u, bool acc) {
+      const int st = u % kNS, pb = u & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u))) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        for (int ks = 0; ks < 8; ++ks)
+          mma_f16_ss(tmem + 32, desc_mnmajor_sw128(smem_addr(sm.v[st]) + ks * 2048, kBox, 1024),
+                     desc_kmajor_sw128(smem_addr(sm.pt[pb] + (ks >> 2) * kRowBox) + (ks & 3) * 32), kIdO,
+                     acc || ks > 0);
+        mma_commit(&sm.p_free[pb]);
+        mma_commit(&sm.empty[st]);
+      }
+      __syncwarp();
+      return true;
+    };
+    while (ok) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.ifull[slot], iphase[slot]))) {
+        ok = false;
+        break;
+      }
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      for (int t = 0; t < it.ntiles && ok; ++t) {
+        const int u = tau + t, st = u % kNS, sb = u & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[st], (uint32_t)(u / kNS) & 1u) &&
+                                         mbar_wait(&sm.s_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t koff = (ks & 3) * 32;
+            mma_f16_ss(tmem + sb * 16, desc_kmajor_sw128(smem_addr(sm.k[st] + (ks >> 2) * kBox) + koff),
+                       desc_kmajor_sw128(smem_addr(sm.qt[slot] + (ks >> 2) * kRowBox) + koff), kIdS, ks > 0);
+          }
+          mma_commit(&sm.s_full[sb]);
+        }
+        __syncwarp();
+        if (t > 0 && !issue_pv(u - 1, t - 1 > 0)) ok = false;
+      }
+      if (ok && it.ntiles > 0 && !issue_pv(tau + it.ntiles - 1, it.ntiles > 1)) ok = false;
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&sm.o_full);
+        mma_commit(&sm.iempty[slot]);
+      }
+      __syncwarp();
+      tau += it.ntiles;
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+      if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+    if (lane == 0) {
+      mma_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax
+    // A warp never leaves the loop except right after a named barrier at
+    // which every softmax warp reads the same abort flag.
+    const int quarter = warp & 3;
+    const int kl = quarter * 32 + lane;           // tensor-memory lane: key of the tile, dim of O^T
+    const int ws = warp - kSoftWarp0;             // softmax warp index 0..3
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int rows = p.S * p.G;
+    int slot = 0, tau = 0, icount = 0;
+    uint32_t iphase[2] = {0, 0};
+    while (true) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.ifull[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
+      named_sync();
+      if (aborted(sm)) break;
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      const int b = it.b, g = it.g;
+      int pos_r[R], ih_r[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int i = r < rows ? r / p.G : 0;
+        pos_r[r] = it.past + i;
+        ih_r[r] = r < rows ? i * p.N + g * p.G + r % p.G : -1;
+      }
+      float m_run[R], l_part[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        m_run[r] = kNegBig;
+        l_part[r] = 0.f;
+      }
+      bool bad = false;
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int u = tau + t, sb = u & 1, st = u % kNS;
+        const int jk = it.j0 + t * kKT + kl;      // this thread's key
+        const bool key_ok = jk < it.jend;
+        float s[R];
+        bool got = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (uint32_t)(u >> 1) & 1u));
+        if (got) {
+          tc_fence_after();
+          uint32_t raw[16];
+          tmem_ld16(tmem + lane_addr + sb * 16, raw);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&sm.s_free[sb]);
+          // V rows past the key range may hold any bits: zero them (P is 0 there, 0 * NaN is not).
+          if (!key_ok) {
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(sm.v[st] + bx * kBox + kl * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float x = __uint_as_float(raw[r]);
+            bool vis = key_ok && ih_r[r] >= 0;
+            if (p.causal) vis = vis && jk <= pos_r[r];
+            if (p.window >= 0) vis = vis && jk >= pos_r[r] - p.window;
+            if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap) * kLog2e;
+            if (p.has_bias && vis) {
+              const int i = ih_r[r] / p.N, h = ih_r[r] % p.N;
+              const long long bi =
+                  (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
+                      p.bias_ld + jk;
+              x += load_t(p.bias, bi, p.t_type) * kLog2e;
+            }
+            s[r] = vis ? x : kNegBig;
+            float m = s[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) sm.red[sb][ws][r] = m;
+          }
+        } else if (lane == 0) {
+          set_abort(p, sm);
+        }
+        named_sync();
+        if (aborted(sm)) {
+          bad = true;
+          break;
+        }
+        // Tile max per row; lazy rescale of O^T (only after the item's first tile).
+        float mt[R];
+        bool any_grow = false;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          mt[r] = fmaxf(fmaxf(sm.red[sb][0][r], sm.red[sb][1][r]), fmaxf(sm.red[sb][2][r], sm.red[sb][3][r]));
+          any_grow = any_grow || mt[r] > m_run[r] + kLazy;
+        }
+        if (any_grow && t > 0) {
+          // O^T must hold P.V up to tile t-1.
+          const int pu = u - 1;
+          if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[pu & 1], (uint32_t)(pu >> 1) & 1u))) {
+            tc_fence_after();
+            uint32_t o[16];
+            tmem_ld16(tmem + lane_addr + 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              if (mt[r] > m_run[r] + kLazy) {
+                const float f = ex2(m_run[r] - mt[r]);
+                o[r] = __float_as_uint(__uint_as_float(o[r]) * f);
+                l_part[r] *= f;
+              }
+            }
+            tmem_st16(tmem + lane_addr + 32, o);
+            tmem_st_wait();
+          } else if (lane == 0) {
+            set_abort(p, sm);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (mt[r] > m_run[r] + kLazy) m_run[r] = mt[r];
+        // P^T(u): its buffer is free once P.V(u-2) finished.
+        if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float pr = s[r] <= kNegBig ? 0.f : ex2(s[r] - m_run[r]);
+            l_part[r] += pr;
+            *reinterpret_cast<__half*>(sm.pt[sb] + sw_elem(r, kl, kRowBox)) = __float2half_rn(pr);
+          }
+        } else if (lane == 0) {
+          set_abort(p, sm);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[sb]);
+      }
+      if (bad) break;
+      tau += it.ntiles;
+      // ---- end of item: O^T row kl = dim kl of every query row
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.o_full, (uint32_t)icount & 1u));
+      uint32_t o[16];
+      if (got) {
+        tc_fence_after();
+        tmem_ld16(tmem + lane_addr + 32, o);
+        tmem_ld_wait();
+      } else if (lane == 0) {
+        set_abort(p, sm);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float l = l_part[r];
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
+        if (lane == 0) sm.redl[ws][r] = l;
+      }
+      named_sync();
+      if (aborted(sm)) break;
+      const int bg = b * p.Nkv + g;
+      if (it.nsplit == 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r >= rows) continue;
+          const float l = sm.redl[0][r] + sm.redl[1][r] + sm.redl[2][r] + sm.redl[3][r];
+          write_out(p, b, g, it.total, r, kl, m_run[r], l, __uint_as_float(o[r]));
+        }
+      } else {
+        const long long pbase = (long long)it.slot * p.rows_pad;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r >= rows) continue;
+          p.part_o[(pbase + r) * kHD + kl] = __uint_as_float(o[r]);
+          if (kl == 0) {
+            p.part_ml[(pbase + r) * 2] = m_run[r];
+            p.part_ml[(pbase + r) * 2 + 1] = sm.redl[0][r] + sm.redl[1][r] + sm.redl[2][r] + sm.redl[3][r];
+          }
+        }
+        named_sync();
+        if (tid == kSoftWarp0 * 32) {   // first softmax thread
+          const unsigned ticket = ticket_acq_rel(&p.counters[bg]);
+          sm.last = ticket == (unsigned)(it.nsplit - 1);
+        }
+        named_sync();
+        if (sm.last) {
+          // One pass over the splits (online merge); the loads of a split for
+          // all rows are independent, so they are in flight together.
+          float M[R], Ls[R], A[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            M[r] = kNegBig;
+            Ls[r] = 0.f;
+            A[r] = 0.f;
+          }
+          for (int s2 = 0; s2 < it.nsplit; ++s2) {
+            const long long sb0 = (long long)(s2 == 0 ? it.slot0 : 2 * (it.cfirst + s2)) * p.rows_pad;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              if (r >= rows) continue;
+              const float m = __ldcg(&p.part_ml[(sb0 + r) * 2]);
+              const float l = __ldcg(&p.part_ml[(sb0 + r) * 2 + 1]);
+              const float ov = __ldcg(&p.part_o[(sb0 + r) * kHD + kl]);
+              const float mn = fmaxf(M[r], m);
+              const float fa = ex2(M[r] - mn), fb = ex2(m - mn);
+              Ls[r] = Ls[r] * fa + l * fb;
+              A[r] = A[r] * fa + ov * fb;
+              M[r] = mn;
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            if (r < rows) write_out(p, b, g, it.total, r, kl, M[r], Ls[r], A[r]);
+          if (tid == kSoftWarp0 * 32) p.counters[bg] = 0;  // ready for the next call
+        }
+        named_sync();
+        if (tid == kSoftWarp0 * 32) sm.last = 0;
+      }
+      named_sync();   // slot, reduction buffers and the ticket flag are free again
+      if (tid == kSoftWarp0 * 32) mbar_arrive(&sm.iempty[slot]);
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+      ++icount;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 64);
+}
+
+template <int R>
+cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv) {
+  const int smem = (int)sizeof(DSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int grid = sms < kTcDecodeMaxCtas ? sms : kTcDecodeMaxCtas;
+  decode_tc_kernel<R><<<grid, kThreads, smem, st>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_supported(const Params& p) {
+  return p.t_type == kF16 && p.cache_type == kF16 && p.H == kHD && p.S * p.G <= kNR;
+}
+
+cudaError_t launch_decode_tc(const Params& p, cudaStream_t st) {
+  const long long krows = (long long)p.B * p.Nkv * p.C;
+  CUtensorMap mk, mv;
+  cudaError_t e = encode_fp16_2d_sw128(&mk, p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kKT);
+  if (e != cudaSuccess) return e;
+  if ((e = encode_fp16_2d_sw128(&mv, p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kKT)) != cudaSuccess) return e;
+  switch (p.rows_pad) {
+    case 1: return launch_r<1>(p, st, mk, mv);
+    case 2: return launch_r<2>(p, st, mk, mv);
+    case 4: return launch_r<4>(p, st, mk, mv);
+    case 8: return launch_r<8>(p, st, mk, mv);
+    case 16: return launch_r<16>(p, st, mk, mv);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gqa

@@ -46,21 +46,11 @@ gqa_status fail(gqa_status s, const char* fmt, ...) {
 }
 
 constexpr size_t kAlign = 256;
-constexpr int kDecodeMaxRows = 8;
 constexpr long long kDecodeTargetCtas = 152LL * 16;  // GB300: 152 SMs, ~16 split CTAs per SM
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool present(const gqa_tensor& t) { return t.data != nullptr; }
-
-int elem_size(int dt) {
-  switch (dt) {
-    case GQA_F32: case GQA_I32: return 4;
-    case GQA_F16: case GQA_BF16: return 2;
-    case GQA_I8: case GQA_U8: return 1;
-    default: return 0;
-  }
-}
 
 bool shape_is(const gqa_tensor& t, int ndim, const int64_t* s) {
   if (t.ndim != ndim) return false;
@@ -82,7 +72,9 @@ struct Plan {
   gqa::Params P;
   bool decode;
   bool tensor_core;  // prefill on the tcgen05 kernel (fp16, head size 128)
+  bool tc_decode;    // decode on the tcgen05 kernel (fp16 cache, head size 128, <= 16 rows)
   size_t hdr_bytes, qprep_bytes, part_bytes, total_bytes;
+  size_t part_rows;  // decode partial rows (part_o holds part_rows x H floats, part_ml part_rows x 2)
 };
 
 gqa_status check_aligned(const gqa_tensor& t, const char* name) {
@@ -279,21 +271,34 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.out = out->output.data;
 
   // ---- regime and workspace plan
-  pl->decode = gqa::decode_supported(P);
+  pl->decode = gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P));
+  pl->tc_decode = pl->decode && gqa::decode_tc_supported(P);
   pl->tensor_core = false;
-  pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));
+  pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));  // status, tickets
   pl->qprep_bytes = 0;
   pl->part_bytes = 0;
+  pl->part_rows = 0;
   if (pl->decode) {
     int rp = 1;
     while (rp < S * G) rp <<= 1;
     P.rows_pad = rp;
-    long long L = 64;
-    const long long work = B * Nkv * T;
-    while (L < 4096 && work / L > kDecodeTargetCtas) L <<= 1;
-    P.split_len = (int)L;
-    P.max_splits = (int)((T + L - 1) / L);
-    const size_t nb = (size_t)B * Nkv * P.max_splits * rp;
+    size_t nb;
+    if (pl->tc_decode) {
+      // Balanced decomposition: every CTA takes an equal share of the 128-key
+      // tiles of all (b, g) ranges; at most its first and last segment are
+      // shared with another CTA and need a partial slot.
+      P.split_len = gqa::kTcDecodeTile;
+      P.max_splits = 2 * gqa::kTcDecodeMaxCtas;
+      nb = (size_t)P.max_splits * rp;
+    } else {
+      long long L = 64;
+      const long long work = B * Nkv * T;
+      while (L < 4096 && work / L > kDecodeTargetCtas) L <<= 1;
+      P.split_len = (int)L;
+      P.max_splits = (int)((T + L - 1) / L);
+      nb = (size_t)B * Nkv * P.max_splits * rp;
+    }
+    pl->part_rows = nb;
     pl->part_bytes = align_up(nb * H * sizeof(float)) + align_up(nb * 2 * sizeof(float));
   } else {
     if (!gqa::prefill_simt_supported(P) || !gqa::prepass_supported(P))
@@ -317,9 +322,8 @@ void bind_workspace(Plan* pl, void* ws) {
     cur += pl->qprep_bytes;
   }
   if (pl->part_bytes) {
-    const size_t nb = (size_t)P.B * P.Nkv * P.max_splits * P.rows_pad;
     P.part_o = reinterpret_cast<float*>(cur);
-    P.part_ml = reinterpret_cast<float*>(cur + align_up(nb * P.H * sizeof(float)));
+    P.part_ml = reinterpret_cast<float*>(cur + align_up(pl->part_rows * P.H * sizeof(float)));
   }
 }
 
@@ -436,7 +440,8 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
   if (pl.decode) {
-    e = timed_launch(h, GQA_KERNEL_DECODE, st, [&] { return gqa::launch_decode(P, st); });
+    e = timed_launch(h, GQA_KERNEL_DECODE, st,
+                     [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st) : gqa::launch_decode(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   } else {
     e = timed_launch(h, GQA_KERNEL_PREPASS, st, [&] { return gqa::launch_prepass(P, st); });
@@ -472,7 +477,8 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
-  e = timed_launch(h, GQA_KERNEL_DECODE, st, [&] { return gqa::launch_decode(P, st); });
+  e = timed_launch(h, GQA_KERNEL_DECODE, st,
+                   [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st) : gqa::launch_decode(P, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return GQA_OK;
 }

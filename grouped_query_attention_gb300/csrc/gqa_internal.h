@@ -56,10 +56,11 @@ struct Params {
   void* qprep;           // prepared queries, layout [B][N_kv][S*G][H]
   int qprep_type;        // ElemType of qprep
   float* part_o;         // decode partial outputs [B*N_kv][max_splits][R][H]
-  float* part_ml;        // decode partial (m, l)   [B*N_kv][max_splits][R][2]
+                         // (tensor-core decode: [max_splits][R][H], one slot per CTA segment)
+  float* part_ml;        // decode partial (m, l)   [B*N_kv][max_splits][R][2] (same note)
   unsigned int* counters;  // decode merge tickets  [B*N_kv]
-  int split_len;         // keys per decode split
-  int max_splits;        // grid extent of the split axis
+  int split_len;         // keys per decode split (tensor-core decode: keys per balanced unit)
+  int max_splits;        // grid extent of the split axis (tensor-core decode: partial slots)
   int rows_pad;          // R: decode rows per (b, g) rounded to a power of two
 };
 
@@ -83,6 +84,12 @@ cudaError_t noalloc_scratch(void** ptr);
 cudaError_t launch_copy_past(const Params& p, cudaStream_t st);
 cudaError_t launch_prepass(const Params& p, cudaStream_t st);
 cudaError_t launch_decode(const Params& p, cudaStream_t st);
+cudaError_t launch_decode_tc(const Params& p, cudaStream_t st);
+// The tensor-core decode runs min(SM count, kTcDecodeMaxCtas) persistent CTAs
+// and keeps two partial slots per CTA.
+constexpr int kTcDecodeMaxCtas = 256;
+constexpr int kTcDecodeTile = 128;
+bool decode_tc_supported(const Params& p);
 cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st);
 cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st);
 bool prefill_tc_supported(const Params& p);

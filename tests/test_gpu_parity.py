@@ -1,8 +1,9 @@
 """GPU parity: the CUDA library (through the C ABI) against the fp64 oracle.
 
 Tiny sweeps cover every feature and cache mode, several splits / tiles and a
-ragged tail in both regimes (fused split-KV decode for S*G <= 8, pre-pass +
-flash prefill otherwise). The five workloads run at full size with the
+ragged tail in both regimes (fused split-KV decode for up to 8 query rows per
+KV head, or 16 on the tensor-core decode; pre-pass + flash prefill
+otherwise). The five workloads run at full size with the
 launch configuration the benchmark uses; their outputs are checked on
 sampled rows the oracle computes one by one and their caches in full.
 """
@@ -40,6 +41,18 @@ DECODE = {
     "f16_window_zero": spec(local_window_size=0),
     "f32_bidirectional_prompt": spec(dtype="f32", mode="prompt", capacity=1, S=1, N=4, Nkv=1, causal=0,
                                      seqlens_k=(0, 0, 0), seqlens_range=None),
+    # tensor-core decode (fp16, head size 128): 16 query rows per KV head, every feature
+    "f16_tc_r16_all_features": spec(N=16, Nkv=2, S=2, capacity=1200, seqlens_range=(1, 1100),
+                                    local_window_size=300, softcap=20.0, bias=(3, 16, 0.5), head_sink=True,
+                                    qk_norm=True, rotary_theta=1e4),
+    "f16_tc_r16_smooth_short": spec(N=16, Nkv=1, S=1, capacity=300, seqlens_range=(0, 299), smooth_softmax=1),
+    # one (b, g) spread over every CTA: a merge of one partial per CTA
+    "f16_tc_one_head_long": spec(B=1, N=8, Nkv=1, capacity=40000, seqlens_range=(39000, 39990), rotary_theta=1e4),
+    # fewer tiles than CTAs (only the first CTAs work)
+    "f16_tc_few_tiles": spec(B=2, N=4, Nkv=2, capacity=200, seqlens_range=(0, 150)),
+    # new rows straddling a 128-key tile boundary (keys 1022..1025), S*G = 16
+    "f16_tc_s4_straddle": spec(S=4, N=16, Nkv=4, capacity=1100, seqlens_k=(1025, 130, 3), seqlens_range=None,
+                               rotary_theta=1e4, qk_norm=True),
 }
 
 PREFILL = {
