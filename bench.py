@@ -274,13 +274,20 @@ def run_gpu_arm(args, world, rank, local) -> None:
     plan = op.plan(**call)
     ws = torch.empty(max(int(plan.workspace_bytes), 256), dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_words = flush.view(torch.int32)
+
+    def flush_l2():
+        # Write a buffer larger than L2, then read it back, so that the timed
+        # step starts with an L2 holding none of its data and no dirty lines.
+        flush.zero_()
+        flush_words.sum()
     stream = torch.cuda.current_stream(device)
 
     def step():
         op(workspace=ws, **call)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     assert op.device_status() == 0, "device status set during warm-up"
@@ -292,7 +299,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     soak_end = time.perf_counter() + args.soak
     while time.perf_counter() < soak_end:
         for _ in range(20):
-            flush.zero_()
+            flush_l2()
             step()
         torch.cuda.synchronize()
 
@@ -304,7 +311,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     # over exactly the timed steps: the roofline uses the dominant kernel's time.
     capi.gqa_profile_begin(op.handle, args.steps * int(plan.launches))
     for k in range(args.steps):
-        flush.zero_()                      # L2 flush between timed iterations
+        flush_l2()                         # L2 flush between timed iterations
         starts[k].record(stream)
         step()
         ends[k].record(stream)
@@ -332,7 +339,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     barrier(world)
     torch.cuda.synchronize()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         e_starts[k].record(stream)
         for name, t in host_in.items():
             dev[name].copy_(t, non_blocking=True)
@@ -385,7 +392,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
         "config": {"workload": args.workload, "batch": sp.B, "seq_len": sp.S, "num_heads": sp.N,
                    "kv_num_heads": sp.Nkv, "head_size": sp.H, "capacity": sp.capacity,
                    "cache": sp.quant if sp.quant != "NONE" else sp.dtype,
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then read back)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "regime": "decode" if plan.regime == 1 else "prefill",
                    "split_len": int(plan.split_len), "max_splits": int(plan.max_splits)},

@@ -81,8 +81,8 @@ struct __align__(1024) DSmem {
   float red[2][4][kNR];         // cross-warp row max, double-buffered by tile parity
   float redl[4][kNR];           // cross-warp row sum
   DItem item[2];
-  uint64_t full[kNS], empty[kNS];
-  uint64_t ifull[2], iempty[2];
+  uint64_t kfull[kNS], kempty[kNS], vfull[kNS], vempty[kNS];
+  uint64_t imap[2], iready[2], iempty[2];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full;
   uint64_t drain;
@@ -255,21 +255,63 @@ __device__ __forceinline__ void norm_rope(const Params& p, float* x, const void*
 }
 
 // The group's query rows of an item as fp16 MMA operand rows (scaled into the
-// log2 domain unless softcap). Rows >= R stay zero from the kernel start.
+// log2 domain unless softcap). Rows >= R stay zero from the kernel start. All
+// loads are issued before the arithmetic, so their latencies overlap.
+template <int R>
 __device__ void prepare_qt(const Params& p, const DItem& it, uint8_t* qt) {
   const int lane = threadIdx.x & 31;
   const int rows = p.S * p.G;
   const float qscale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
-  for (int r = 0; r < rows; ++r) {
+  const __half* q = reinterpret_cast<const __half*>(p.q);
+  const __half* cosc = reinterpret_cast<const __half*>(p.cos_c);
+  const __half* sinc = reinterpret_cast<const __half*>(p.sin_c);
+  float x[R][4], cs[R][2], sn[R][2], w[4];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (r >= rows) continue;
     const int i = r / p.G, h = it.g * p.G + r % p.G;
     const long long src = ((long long)(it.b * p.S + i) * p.N + h) * kHD;
-    float x[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = load_t(p.q, src + lane + 32 * e, p.t_type);
-    norm_rope(p, x, p.qw, it.past + i, p.has_norm, p.has_rotary);
+    for (int e = 0; e < 4; ++e) x[r][e] = __half2float(q[src + lane + 32 * e]);
+    if (p.has_rotary) {
+      const long long cbase = (long long)(it.past + i) * (kHD / 2);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        cs[r][e] = __half2float(cosc[cbase + lane + 32 * e]);
+        sn[r][e] = __half2float(sinc[cbase + lane + 32 * e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    w[e] = p.has_norm ? __half2float(reinterpret_cast<const __half*>(p.qw)[lane + 32 * e]) : 1.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (r >= rows) continue;
+    float* v = x[r];
+    if (p.has_norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss += v[e] * v[e];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rn = 1.0f / sqrtf(ss / (float)kHD + p.eps);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = (v[e] * rn) * w[e];
+    }
+    if (p.has_rotary) {
+      float y[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        y[e] = v[e] * cs[r][e] - v[e + 2] * sn[r][e];
+        y[e + 2] = v[e + 2] * cs[r][e] + v[e] * sn[r][e];
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = y[e];
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      *reinterpret_cast<__half*>(qt + sw_elem(r, lane + 32 * e, kRowBox)) = __float2half_rn(x[e] * qscale);
+      *reinterpret_cast<__half*>(qt + sw_elem(r, lane + 32 * e, kRowBox)) = __float2half_rn(v[e] * qscale);
   }
 }
 
@@ -333,11 +375,14 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
   if (warp == 1) tmem_alloc(&sm.tmem, 64);
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.kfull[s], 1);
+      mbar_init(&sm.kempty[s], 1);
+      mbar_init(&sm.vfull[s], 1);
+      mbar_init(&sm.vempty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.ifull[s], 1);
+      mbar_init(&sm.imap[s], 1);
+      mbar_init(&sm.iready[s], 1);
       mbar_init(&sm.iempty[s], 2);  // MMA commit (Q^T reads done) + softmax release
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.s_free[s], kSoft);
@@ -384,7 +429,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (t >= tend) {
         if (lane == 0) {
           sm.item[slot].end = 1;
-          mbar_arrive(&sm.ifull[slot]);
+          mbar_arrive(&sm.imap[slot]);
+          mbar_arrive(&sm.iready[slot]);
         }
         break;
       }
@@ -395,50 +441,78 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         break;
       }
       t += it.ntiles;
-      if (lane == 0) sm.item[slot] = it;
-      prepare_qt(p, it, sm.qt[slot]);
+      // The TMA warp may stream the segment's cached tiles while the query
+      // rows are prepared; tiles holding new rows wait for `iready`.
+      if (lane == 0) {
+        sm.item[slot] = it;
+        mbar_arrive(&sm.imap[slot]);
+      }
+      prepare_qt<R>(p, it, sm.qt[slot]);
       append_rows(p, it);
       fence_async_all();  // query rows (shared) and appended rows (global) -> async proxy
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.ifull[slot]);
+      if (lane == 0) mbar_arrive(&sm.iready[slot]);
       iphase[slot] ^= 1u;
       slot ^= 1;
     }
     if (!ok && lane == 0) set_abort(p, sm);
   } else if (warp == 0) {
     // ================================================================ TMA
-    int slot = 0, tau = 0;
+    // K and V tiles have their own stages: K(u) is released as soon as
+    // S(u) is done, V(u) after O += V P(u).
+    int slot = 0, tau = 0, nk = 0, nv = 0;   // tiles begun; K and V fills issued
     uint32_t iphase[2] = {0, 0};
     bool ok = true;
     while (ok) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.ifull[slot], iphase[slot]))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.imap[slot], iphase[slot]))) {
         ok = false;
         break;
       }
       const DItem it = sm.item[slot];
       if (it.end) break;
-      iphase[slot] ^= 1u;
-      slot ^= 1;
       const int row0 = (it.b * p.Nkv + it.g) * p.C + it.j0;
+      bool ready = false;
       for (int t = 0; t < it.ntiles; ++t, ++tau) {
         const int st = tau % kNS;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.empty[st], ((uint32_t)(tau / kNS) & 1u) ^ 1u)) || aborted(sm)) {
+        const uint32_t par = ((uint32_t)(tau / kNS) & 1u) ^ 1u;
+        if (!ready && it.j0 + (t + 1) * kKT > it.past) {   // the tile holds new rows
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot]))) {
+            ok = false;
+            break;
+          }
+          ready = true;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kempty[st], par)) || aborted(sm)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          mbar_arrive_tx(&sm.full[st], 2 * kTile);
-          for (int bx = 0; bx < 2; ++bx) {
-            tma_load_2d(sm.k[st] + bx * kBox, &tmk, bx * 64, row0 + t * kKT, &sm.full[st]);
-            tma_load_2d(sm.v[st] + bx * kBox, &tmv, bx * 64, row0 + t * kKT, &sm.full[st]);
-          }
+          mbar_arrive_tx(&sm.kfull[st], kTile);
+          tma_load_2d(sm.k[st], &tmk, 0, row0 + t * kKT, &sm.kfull[st]);
+          tma_load_2d(sm.k[st] + kBox, &tmk, 64, row0 + t * kKT, &sm.kfull[st]);
         }
         __syncwarp();
+        ++nk;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vempty[st], par)) || aborted(sm)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_tx(&sm.vfull[st], kTile);
+          tma_load_2d(sm.v[st], &tmv, 0, row0 + t * kKT, &sm.vfull[st]);
+          tma_load_2d(sm.v[st] + kBox, &tmv, 64, row0 + t * kKT, &sm.vfull[st]);
+        }
+        __syncwarp();
+        ++nv;
       }
+      iphase[slot] ^= 1u;
+      slot ^= 1;
     }
     if (!ok && lane == 0) set_abort(p, sm);
-    // Drain: every tile this warp issued has landed before the CTA can exit.
-    for (int u = max(0, tau - kNS); u < tau; ++u) mbar_wait(&sm.full[u % kNS], (uint32_t)(u / kNS) & 1u);
+    // Drain: every fill this warp issued has landed before the CTA can exit
+    // (older fills completed before their stage was refilled).
+    for (int u = max(0, nk - kNS); u < nk; ++u) mbar_wait(&sm.kfull[u % kNS], (uint32_t)(u / kNS) & 1u);
+    for (int u = max(0, nv - kNS); u < nv; ++u) mbar_wait(&sm.vfull[u % kNS], (uint32_t)(u / kNS) & 1u);
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     int slot = 0, tau = 0;
@@ -446,7 +520,9 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     bool ok = true;
     auto issue_pv = [&](int u, bool acc) {
       const int st = u % kNS, pb = u & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u))) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
+                                       mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u)))
+        return false;
       if (lane == 0) {
         tc_fence_after();
         for (int ks = 0; ks < 8; ++ks)
@@ -454,13 +530,13 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
                      desc_kmajor_sw128(smem_addr(sm.pt[pb] + (ks >> 2) * kRowBox) + (ks & 3) * 32), kIdO,
                      acc || ks > 0);
         mma_commit(&sm.p_free[pb]);
-        mma_commit(&sm.empty[st]);
+        mma_commit(&sm.vempty[st]);
       }
       __syncwarp();
       return true;
     };
     while (ok) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.ifull[slot], iphase[slot]))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot]))) {
         ok = false;
         break;
       }
@@ -468,7 +544,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (it.end) break;
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int u = tau + t, st = u % kNS, sb = u & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.full[st], (uint32_t)(u / kNS) & 1u) &&
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[st], (uint32_t)(u / kNS) & 1u) &&
                                          mbar_wait(&sm.s_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
           ok = false;
           break;
@@ -481,6 +557,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
                        desc_kmajor_sw128(smem_addr(sm.qt[slot] + (ks >> 2) * kRowBox) + koff), kIdS, ks > 0);
           }
           mma_commit(&sm.s_full[sb]);
+          mma_commit(&sm.kempty[st]);
         }
         __syncwarp();
         if (t > 0 && !issue_pv(u - 1, t - 1 > 0)) ok = false;
@@ -515,7 +592,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     int slot = 0, tau = 0, icount = 0;
     uint32_t iphase[2] = {0, 0};
     while (true) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.ifull[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
       named_sync();
       if (aborted(sm)) break;
       const DItem it = sm.item[slot];
@@ -549,7 +626,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           tc_fence_before();
           mbar_arrive(&sm.s_free[sb]);
           // V rows past the key range may hold any bits: zero them (P is 0 there, 0 * NaN is not).
-          if (!key_ok) {
+          if (!key_ok && !mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u)) set_abort(p, sm);
+          if (!key_ok && !aborted(sm)) {
 #pragma unroll
             for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
@@ -723,14 +801,30 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
   if (warp == 1) tmem_dealloc(tmem, 64);
 }
 
+// Per-device launch facts, looked up on the first launch on each device
+// (racing first calls store the same values).
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+bool g_smem_set[5][kMaxDevices];
+
 template <int R>
-cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv) {
+cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv, int ri) {
   const int smem = (int)sizeof(DSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_smem_set[ri][dev]) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    g_smem_set[ri][dev] = true;
+  }
+  if (g_sm_count[dev] == 0) {
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    g_sm_count[dev] = sms;
+  }
+  const int sms = g_sm_count[dev];
   const int grid = sms < kTcDecodeMaxCtas ? sms : kTcDecodeMaxCtas;
   decode_tc_kernel<R><<<grid, kThreads, smem, st>>>(p, mk, mv);
   return cudaGetLastError();
@@ -749,11 +843,11 @@ cudaError_t launch_decode_tc(const Params& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if ((e = encode_fp16_2d_sw128(&mv, p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kKT)) != cudaSuccess) return e;
   switch (p.rows_pad) {
-    case 1: return launch_r<1>(p, st, mk, mv);
-    case 2: return launch_r<2>(p, st, mk, mv);
-    case 4: return launch_r<4>(p, st, mk, mv);
-    case 8: return launch_r<8>(p, st, mk, mv);
-    case 16: return launch_r<16>(p, st, mk, mv);
+    case 1: return launch_r<1>(p, st, mk, mv, 0);
+    case 2: return launch_r<2>(p, st, mk, mv, 1);
+    case 4: return launch_r<4>(p, st, mk, mv, 2);
+    case 8: return launch_r<8>(p, st, mk, mv, 3);
+    case 16: return launch_r<16>(p, st, mk, mv, 4);
     default: return cudaErrorInvalidValue;
   }
 }
