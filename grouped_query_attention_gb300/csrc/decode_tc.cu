@@ -155,28 +155,37 @@ __device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, in
   return (total - kstart + kKT - 1) / kKT;
 }
 
-// Number of tiles over all (b, g) (whole warp).
-__device__ long long count_tiles(const Params& p, bool flag_bad) {
+// Work units of a (b, g) with `tiles` tiles: one per tile plus kEndUnits for
+// the end of its key range (the epilogue that writes the output or a partial
+// costs about as much as that many tiles). Shares are equal in units, so a
+// CTA that ends more key ranges gets fewer tiles.
+constexpr int kEndUnits = 5;
+__device__ __forceinline__ long long bg_units(int tiles) { return tiles > 0 ? tiles + kEndUnits : 0; }
+
+// Number of work units over all (b, g) (whole warp).
+__device__ long long count_units(const Params& p, bool flag_bad) {
   const int lane = threadIdx.x & 31;
   long long n = 0;
   for (int b = lane; b < p.B; b += 32) {
     int past, total;
-    n += (long long)batch_tiles(p, b, past, total, flag_bad) * p.Nkv;
+    n += bg_units(batch_tiles(p, b, past, total, flag_bad)) * p.Nkv;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
   return n;
 }
 
-// CTA owning global tile t when `ntot` tiles are shared by `nc` <= ntot CTAs
+// CTA owning global unit t when `ntot` units are shared by `nc` <= ntot CTAs
 // (CTA c owns [c*ntot/nc, (c+1)*ntot/nc), never empty).
 __device__ __forceinline__ long long share_start(long long c, long long ntot, long long nc) { return c * ntot / nc; }
 __device__ __forceinline__ int tile_owner(long long t, long long ntot, long long nc) {
   return (int)(((t + 1) * nc - 1) / ntot);
 }
 
-// The segment that starts at global tile t and ends at min(tend, end of its
-// (b, g)), with a warp-wide prefix scan of the per-batch tile counts.
+// The segment that starts at global unit t and ends at min(tend, last tile of
+// its (b, g)), with a warp-wide prefix scan of the per-batch unit counts. A
+// unit past the last tile of its (b, g) gives end = 2 and, in ntiles, the
+// units to skip to the next (b, g).
 __device__ void map_segment(const Params& p, long long t, long long tend, long long ntot, long long nc,
                             DItem& it) {
   const int lane = threadIdx.x & 31;
@@ -185,7 +194,7 @@ __device__ void map_segment(const Params& p, long long t, long long tend, long l
     const int b = b0 + lane;
     int past = -1, total = 0, tb = 0;
     if (b < p.B) tb = batch_tiles(p, b, past, total, false);
-    const long long n = (long long)tb * p.Nkv;
+    const long long n = bg_units(tb) * p.Nkv;
     long long incl = n;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -200,9 +209,15 @@ __device__ void map_segment(const Params& p, long long t, long long tend, long l
       const int tt = __shfl_sync(0xffffffffu, total, src);
       const int tiles = __shfl_sync(0xffffffffu, tb, src);
       const long long r = t - __shfl_sync(0xffffffffu, excl, src);
+      const int blk = (int)bg_units(tiles);
       it.b = __shfl_sync(0xffffffffu, b, src);
-      it.g = (int)(r / tiles);
-      const int lt = (int)(r % tiles);
+      it.g = (int)(r / blk);
+      const int lt = (int)(r % blk);
+      if (lt >= tiles) {   // end units of the (b, g): nothing to load
+        it.end = 2;
+        it.ntiles = blk - lt;
+        return;
+      }
       const long long first = t - lt, bg_end = first + tiles;
       const long long seg_end = tend < bg_end ? tend : bg_end;
       const int kstart = p.window >= 0 ? max(0, pp - p.window) : 0;
@@ -411,7 +426,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     // With fewer tiles than CTAs only the first `ntot` CTAs work, so that
     // every working CTA's share is non-empty and the CTAs sharing a (b, g)
     // are consecutive.
-    const long long ntot = count_tiles(p, blockIdx.x == 0);
+    const long long ntot = count_units(p, blockIdx.x == 0);
     const long long nc = ntot < (long long)gridDim.x ? ntot : (long long)gridDim.x;
     long long t = 0, tend = 0;
     if ((long long)blockIdx.x < nc) {
@@ -426,6 +441,14 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         ok = false;
         break;
       }
+      DItem it;
+      it.end = 1;
+      while (t < tend) {
+        map_segment(p, t, tend, ntot, nc, it);
+        if (it.end != 2) break;
+        t += it.ntiles;
+        it.end = 1;
+      }
       if (t >= tend) {
         if (lane == 0) {
           sm.item[slot].end = 1;
@@ -434,9 +457,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         }
         break;
       }
-      DItem it;
-      map_segment(p, t, tend, ntot, nc, it);
-      if (it.end) {   // unreachable: every t < ntot maps to a segment
+      if (it.end) {   // unreachable: every t < ntot maps to a unit
         ok = false;
         break;
       }
