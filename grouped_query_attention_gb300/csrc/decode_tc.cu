@@ -387,6 +387,9 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
   DSmem& sm = *reinterpret_cast<DSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // The preparer's first global loads overlap the set-up below.
+  long long ntot = 0;
+  if (warp == 2) ntot = count_units(p, blockIdx.x == 0);
   if (warp == 1) tmem_alloc(&sm.tmem, 64);
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
@@ -426,7 +429,6 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     // With fewer tiles than CTAs only the first `ntot` CTAs work, so that
     // every working CTA's share is non-empty and the CTAs sharing a (b, g)
     // are consecutive.
-    const long long ntot = count_units(p, blockIdx.x == 0);
     const long long nc = ntot < (long long)gridDim.x ? ntot : (long long)gridDim.x;
     long long t = 0, tend = 0;
     if ((long long)blockIdx.x < nc) {
@@ -857,12 +859,16 @@ bool decode_tc_supported(const Params& p) {
   return p.t_type == kF16 && p.cache_type == kF16 && p.H == kHD && p.S * p.G <= kNR;
 }
 
-cudaError_t launch_decode_tc(const Params& p, cudaStream_t st) {
+cudaError_t prepare_decode_tc(const Params& p, TmaMaps* maps) {
   const long long krows = (long long)p.B * p.Nkv * p.C;
-  CUtensorMap mk, mv;
-  cudaError_t e = encode_fp16_2d_sw128(&mk, p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kKT);
+  cudaError_t e = encode_fp16_2d_sw128(&maps->m[0], p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kKT);
   if (e != cudaSuccess) return e;
-  if ((e = encode_fp16_2d_sw128(&mv, p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kKT)) != cudaSuccess) return e;
+  return encode_fp16_2d_sw128(&maps->m[1], p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kKT);
+}
+
+cudaError_t launch_decode_tc(const Params& p, cudaStream_t st, const TmaMaps& maps) {
+  const CUtensorMap& mk = maps.m[0];
+  const CUtensorMap& mv = maps.m[1];
   switch (p.rows_pad) {
     case 1: return launch_r<1>(p, st, mk, mv, 0);
     case 2: return launch_r<2>(p, st, mk, mv, 1);

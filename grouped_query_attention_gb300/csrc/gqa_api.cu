@@ -434,20 +434,26 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
     h->zeroed_bytes = pl.hdr_bytes;
   }
   const gqa::Params& P = pl.P;
-  cudaError_t e;
+  cudaError_t e = cudaSuccess;
+  gqa::TmaMaps maps;   // host work of the tensor-core launches, done before the first launch
+  if (pl.decode && pl.tc_decode)
+    e = gqa::prepare_decode_tc(P, &maps);
+  else if (!pl.decode && pl.tensor_core)
+    e = gqa::prepare_prefill_tc(P, &maps);
+  if (e != cudaSuccess) return cuda_fail(e, "TMA tensor maps");
   if (P.mode == gqa::kCopy) {
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
   if (pl.decode) {
     e = timed_launch(h, GQA_KERNEL_DECODE, st,
-                     [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st) : gqa::launch_decode(P, st); });
+                     [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st, maps) : gqa::launch_decode(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   } else {
     e = timed_launch(h, GQA_KERNEL_PREPASS, st, [&] { return gqa::launch_prepass(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "pre-pass launch");
     if (pl.tensor_core)
-      e = timed_launch(h, GQA_KERNEL_PREFILL_TENSOR_CORE, st, [&] { return gqa::launch_prefill_tc(P, st); });
+      e = timed_launch(h, GQA_KERNEL_PREFILL_TENSOR_CORE, st, [&] { return gqa::launch_prefill_tc(P, st, maps); });
     else
       e = timed_launch(h, GQA_KERNEL_PREFILL_CUDA_CORE, st, [&] { return gqa::launch_prefill_simt(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
@@ -461,7 +467,7 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
   if (s != GQA_OK) return s;
   if (!pl.decode)
     return fail(GQA_ERR_UNSUPPORTED,
-                "gqa_forward_noalloc runs the decode regime only (S*num_heads/kv_num_heads <= 8, head size 64 or 128)");
+                "gqa_forward_noalloc runs the decode regime only (gqa_describe_plan reports the regime)");
   if (pl.total_bytes > gqa::kNoAllocScratchBytes)
     return fail(GQA_ERR_WORKSPACE, "call needs %zu bytes of scratch; the fixed scratch holds %zu (use gqa_forward)",
                 pl.total_bytes, gqa::kNoAllocScratchBytes);
@@ -473,12 +479,14 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
   e = cudaMemsetAsync(scratch, 0, pl.hdr_bytes, st);  // status word and merge tickets start at zero
   if (e != cudaSuccess) return cuda_fail(e, "scratch header clear");
   const gqa::Params& P = pl.P;
+  gqa::TmaMaps maps;
+  if (pl.tc_decode && (e = gqa::prepare_decode_tc(P, &maps)) != cudaSuccess) return cuda_fail(e, "TMA tensor maps");
   if (P.mode == gqa::kCopy) {
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
   e = timed_launch(h, GQA_KERNEL_DECODE, st,
-                   [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st) : gqa::launch_decode(P, st); });
+                   [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st, maps) : gqa::launch_decode(P, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return GQA_OK;
 }

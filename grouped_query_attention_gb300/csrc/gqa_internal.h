@@ -2,6 +2,7 @@
 // kernel translation units. Not part of the public C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -84,14 +85,22 @@ cudaError_t noalloc_scratch(void** ptr);
 cudaError_t launch_copy_past(const Params& p, cudaStream_t st);
 cudaError_t launch_prepass(const Params& p, cudaStream_t st);
 cudaError_t launch_decode(const Params& p, cudaStream_t st);
-cudaError_t launch_decode_tc(const Params& p, cudaStream_t st);
+// TMA tensor maps of a tensor-core launch, encoded on the host before the
+// launch (kept out of the launch itself so nothing but the launch sits
+// between a caller's timing events).
+struct TmaMaps {
+  CUtensorMap m[3];
+};
+cudaError_t prepare_decode_tc(const Params& p, TmaMaps* maps);
+cudaError_t launch_decode_tc(const Params& p, cudaStream_t st, const TmaMaps& maps);
 // The tensor-core decode runs min(SM count, kTcDecodeMaxCtas) persistent CTAs
 // and keeps two partial slots per CTA.
 constexpr int kTcDecodeMaxCtas = 256;
 constexpr int kTcDecodeTile = 128;
 bool decode_tc_supported(const Params& p);
 cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st);
-cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st);
+cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps);
+cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& maps);
 bool prefill_tc_supported(const Params& p);
 bool decode_supported(const Params& p);
 bool prepass_supported(const Params& p);

@@ -487,21 +487,37 @@ bool prefill_tc_supported(const Params& p) {
   return p.t_type == kF16 && p.cache_type == kF16 && p.H == kHD;
 }
 
-cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st) {
+cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps) {
   const long long qrows = (long long)p.B * p.Nkv * p.S * p.G;
   const long long krows = (long long)p.B * p.Nkv * p.C;
-  CUtensorMap mq, mk, mv;
-  cudaError_t e = encode_fp16_2d_sw128(&mq, p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM);
+  cudaError_t e = encode_fp16_2d_sw128(&maps->m[0], p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM);
   if (e != cudaSuccess) return e;
-  if ((e = encode_fp16_2d_sw128(&mk, p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess) return e;
-  if ((e = encode_fp16_2d_sw128(&mv, p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess) return e;
+  if ((e = encode_fp16_2d_sw128(&maps->m[1], p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
+    return e;
+  return encode_fp16_2d_sw128(&maps->m[2], p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kBN);
+}
+
+namespace {
+// Dynamic shared memory opt-in, set once per device and kernel variant.
+constexpr int kMaxDevices = 64;
+bool g_smem_set[2][kMaxDevices];
+}  // namespace
+
+cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& maps) {
   const int smem = (int)sizeof(TcSmem) + 1024;
   const bool plain = p.softcap <= 0.f && !p.has_bias;
   auto kern = plain ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_smem_set[plain][dev]) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    g_smem_set[plain][dev] = true;
+  }
   const int nrows = p.S * p.G;
   dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
-  kern<<<grid, kThreads, smem, st>>>(p, mq, mk, mv);
+  kern<<<grid, kThreads, smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2]);
   return cudaGetLastError();
 }
 
