@@ -180,112 +180,112 @@ prepass_kernel(const Params p) {
   }
 }
 
-// Vectorised pre-pass for rows of at most 32 16-byte chunks: LPR = H / V lanes
-// per row (V elements per 16-byte chunk), 32 / LPR rows per warp. Each lane
-// holds one chunk; the rotary partner (d +- H/2) is chunk lane ^ LPR/2, read
-// with one shuffle per element; norm weights and cos/sin rows are 16-byte
-// vector loads.
+// Vectorised pre-pass for rows of at most 32 16-byte chunks. One block per
+// token (b, i) handles its 2*N_kv + N_q rows (K rows, V rows, query rows);
+// LPR = H / V lanes per row (V elements per 16-byte chunk), 256 / LPR row
+// groups per block, each taking kUnroll rows per pass with their loads issued
+// together. The rotary partner (d +- H/2) is chunk lane ^ LPR/2, read with one
+// shuffle per element; norm weights and cos/sin rows are 16-byte vector loads.
+constexpr int kUnroll = 4;
+
 template <typename T, typename CacheT, typename QT, int H>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 prepass_vec_kernel(const Params p) {
   constexpr int V = Vec<T>::n;
   constexpr int LPR = H / V;            // lanes per row (power of two, <= 32)
-  constexpr int RPW = 32 / LPR;         // rows per warp
+  constexpr int GROUPS = 256 / LPR;     // row groups per block
   static_assert(LPR >= 2 && LPR <= 32 && (LPR & (LPR - 1)) == 0, "row layout");
   const int lane = threadIdx.x & 31;
-  const int sub = lane / LPR, cl = lane % LPR;
-  const long long kv_rows = (long long)p.B * p.S * p.Nkv;
-  const long long q_rows = (long long)p.B * p.S * p.N;
-  const long long nrows = 2 * kv_rows + q_rows;
-  const long long row = ((long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * RPW + sub;
-  const bool have = row < nrows;
-  const unsigned gmask = (LPR == 32) ? 0xffffffffu : (((1u << LPR) - 1u) << (sub * LPR));
-
-  int role = kKey, b = 0, i = 0, head = 0;
-  if (have) {
-    if (row < 2 * kv_rows) {
-      role = row < kv_rows ? kKey : kValue;
-      const long long r = row - (role == kValue ? kv_rows : 0);
-      head = (int)(r % p.Nkv);
-      i = (int)((r / p.Nkv) % p.S);
-      b = (int)(r / ((long long)p.Nkv * p.S));
-    } else {
-      role = kQuery;
-      const long long r = row - 2 * kv_rows;
-      head = (int)(r % p.N);
-      i = (int)((r / p.N) % p.S);
-      b = (int)(r / ((long long)p.N * p.S));
-    }
-  }
-  int past = 0;
-  bool skip = !have;
-  if (have) {
-    const int total = p.seqlens[b] + 1;
-    past = batch_past(p, total);
-    if (past < 0) {
-      if (role == kKey && i == 0 && head == 0 && cl == 0) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
-      skip = true;
-    } else if (p.has_rotary && role != kValue && past + i >= p.rotary_rows) {
-      if (cl == 0) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
-      skip = true;
-    }
-  }
-  // Every lane of a row group takes the same path (same row), so the group's
-  // shuffles below see all their partners.
-  if (skip) return;
-  const int pos = past + i;
+  const int grp = threadIdx.x / LPR, cl = threadIdx.x % LPR;
+  const unsigned gmask = (LPR == 32) ? 0xffffffffu : (((1u << LPR) - 1u) << ((lane / LPR) * LPR));
+  const int tok = blockIdx.x;
+  const int b = tok / p.S, i = tok - b * p.S;
+  const int nrow = 2 * p.Nkv + p.N;
   const int d0 = cl * V;
-  const T* src = role == kQuery
-                     ? reinterpret_cast<const T*>(p.q) + ((long long)(b * p.S + i) * p.N + head) * H
-                     : reinterpret_cast<const T*>(role == kKey ? p.k : p.v) + ((long long)(b * p.S + i) * p.Nkv + head) * H;
-  float x[V];
-  load_vec<T>(src + d0, x);
-  if (role != kValue && p.has_norm) {
-    float ss = 0.f;
+  const T* qsrc = reinterpret_cast<const T*>(p.q) + (long long)tok * p.N * H + d0;
+  const T* ksrc = reinterpret_cast<const T*>(p.k) + (long long)tok * p.Nkv * H + d0;
+  const T* vsrc = reinterpret_cast<const T*>(p.v) + (long long)tok * p.Nkv * H + d0;
+  const int total = p.seqlens[b] + 1;
+
+  for (int r0 = grp; r0 < nrow; r0 += GROUPS * kUnroll) {
+    // Loads of all rows of this pass first (addresses need no lengths), kept
+    // as raw 16-byte chunks until used.
+    uint4 raw[kUnroll];
 #pragma unroll
-    for (int k = 0; k < V; ++k) ss += x[k] * x[k];
-#pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
-    const float r = 1.0f / sqrtf(ss / (float)H + p.eps);
-    float w[V];
-    load_vec<T>(reinterpret_cast<const T*>(role == kQuery ? p.qw : p.kw) + d0, w);
-#pragma unroll
-    for (int k = 0; k < V; ++k) x[k] = (x[k] * r) * w[k];
-  }
-  if (role != kValue && p.has_rotary) {
-    const bool first = cl < LPR / 2;
-    const int dc = (first ? cl : cl - LPR / 2) * V;
-    float c[V], sn[V];
-    load_vec<T>(reinterpret_cast<const T*>(p.cos_c) + (long long)pos * (H / 2) + dc, c);
-    load_vec<T>(reinterpret_cast<const T*>(p.sin_c) + (long long)pos * (H / 2) + dc, sn);
-    float y[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k) {
-      const float xp = __shfl_xor_sync(gmask, x[k], LPR / 2);
-      y[k] = first ? (x[k] * c[k] - xp * sn[k]) : (x[k] * c[k] + xp * sn[k]);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = r0 + u * GROUPS;
+      if (r >= nrow) continue;
+      const T* src = r < p.Nkv ? ksrc + (long long)r * H
+                     : r < 2 * p.Nkv ? vsrc + (long long)(r - p.Nkv) * H
+                                     : qsrc + (long long)(r - 2 * p.Nkv) * H;
+      raw[u] = *reinterpret_cast<const uint4*>(src);
     }
+    const int past = batch_past(p, total);
+    if (past < 0) {
+      if (i == 0 && threadIdx.x == 0 && r0 == grp) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
+      return;   // the whole block (one token) is skipped
+    }
+    const int pos = past + i;
 #pragma unroll
-    for (int k = 0; k < V; ++k) x[k] = y[k];
-  }
-  if (role == kQuery) {
-    const int g = head / p.G, gi = head % p.G;
-    QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
-    store_n<QT, V>(dst, x);
-  } else {
-    const long long off = (((long long)b * p.Nkv + head) * p.C + pos) * H + d0;
-    if constexpr (sizeof(CacheT) == 1) {
-      const float* sc = role == kKey ? p.k_scale : p.v_scale;
-      const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
-      char4 q4[V / 4];
-      int8_t* qb = reinterpret_cast<int8_t*>(q4);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int r = r0 + u * GROUPS;
+      if (r >= nrow) continue;
+      const int role = r < p.Nkv ? kKey : (r < 2 * p.Nkv ? kValue : kQuery);
+      const int head = role == kKey ? r : (role == kValue ? r - p.Nkv : r - 2 * p.Nkv);
+      if (role != kValue && p.has_rotary && pos >= p.rotary_rows) {
+        if (cl == 0) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
+        continue;   // every lane of the row group takes this branch together
+      }
+      float xr[V];
+      load_vec<T>(reinterpret_cast<const T*>(&raw[u]), xr);
+      if (role != kValue && p.has_norm) {
+        float ss = 0.f;
 #pragma unroll
-      for (int k = 0; k < V; ++k) qb[k] = quant_i8(x[k], channel_scale(sc, nsc, head * H + d0 + k));
-      int8_t* dst = reinterpret_cast<int8_t*>(role == kKey ? p.present_k : p.present_v) + off;
-      if constexpr (V == 4) *reinterpret_cast<char4*>(dst) = q4[0];
-      else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
-    } else {
-      CacheT* dst = reinterpret_cast<CacheT*>(role == kKey ? p.present_k : p.present_v) + off;
-      store_n<CacheT, V>(dst, x);
+        for (int k = 0; k < V; ++k) ss += xr[k] * xr[k];
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
+        const float rn = 1.0f / sqrtf(ss / (float)H + p.eps);
+        float w[V];
+        load_vec<T>(reinterpret_cast<const T*>(role == kQuery ? p.qw : p.kw) + d0, w);
+#pragma unroll
+        for (int k = 0; k < V; ++k) xr[k] = (xr[k] * rn) * w[k];
+      }
+      if (role != kValue && p.has_rotary) {
+        const bool first = cl < LPR / 2;
+        const int dc = (first ? cl : cl - LPR / 2) * V;
+        float c[V], sn[V];
+        load_vec<T>(reinterpret_cast<const T*>(p.cos_c) + (long long)pos * (H / 2) + dc, c);
+        load_vec<T>(reinterpret_cast<const T*>(p.sin_c) + (long long)pos * (H / 2) + dc, sn);
+        float y[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          const float xp = __shfl_xor_sync(gmask, xr[k], LPR / 2);
+          y[k] = first ? (xr[k] * c[k] - xp * sn[k]) : (xr[k] * c[k] + xp * sn[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < V; ++k) xr[k] = y[k];
+      }
+      if (role == kQuery) {
+        const int g = head / p.G, gi = head - g * p.G;
+        QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
+        store_n<QT, V>(dst, xr);
+      } else {
+        const long long off = (((long long)b * p.Nkv + head) * p.C + pos) * H + d0;
+        if constexpr (sizeof(CacheT) == 1) {
+          const float* sc = role == kKey ? p.k_scale : p.v_scale;
+          const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
+          char4 q4[V / 4];
+          int8_t* qb = reinterpret_cast<int8_t*>(q4);
+#pragma unroll
+          for (int k = 0; k < V; ++k) qb[k] = quant_i8(xr[k], channel_scale(sc, nsc, head * H + d0 + k));
+          int8_t* dst = reinterpret_cast<int8_t*>(role == kKey ? p.present_k : p.present_v) + off;
+          if constexpr (V == 4) *reinterpret_cast<char4*>(dst) = q4[0];
+          else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
+        } else {
+          CacheT* dst = reinterpret_cast<CacheT*>(role == kKey ? p.present_k : p.present_v) + off;
+          store_n<CacheT, V>(dst, xr);
+        }
+      }
     }
   }
 }
@@ -293,20 +293,19 @@ prepass_vec_kernel(const Params p) {
 template <typename T, typename CacheT, typename QT>
 cudaError_t launch_vec(const Params& p, cudaStream_t st, bool* done) {
   constexpr int V = Vec<T>::n;
-  const long long rows = (long long)p.B * p.S * (2 * p.Nkv + p.N);
-  auto go = [&](auto kern, int lpr) {
-    const int rows_per_block = (256 / 32) * (32 / lpr);
-    const unsigned blocks = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
-    kern<<<blocks, 256, 0, st>>>(p);
+  const long long tokens = (long long)p.B * p.S;
+  auto go = [&](auto kern) {
     *done = true;
+    if (tokens == 0) return cudaSuccess;
+    kern<<<(unsigned)tokens, 256, 0, st>>>(p);
     return cudaGetLastError();
   };
   switch (p.H / V) {
-    case 2: return go(prepass_vec_kernel<T, CacheT, QT, 2 * V>, 2);
-    case 4: return go(prepass_vec_kernel<T, CacheT, QT, 4 * V>, 4);
-    case 8: return go(prepass_vec_kernel<T, CacheT, QT, 8 * V>, 8);
-    case 16: return go(prepass_vec_kernel<T, CacheT, QT, 16 * V>, 16);
-    case 32: return go(prepass_vec_kernel<T, CacheT, QT, 32 * V>, 32);
+    case 2: return go(prepass_vec_kernel<T, CacheT, QT, 2 * V>);
+    case 4: return go(prepass_vec_kernel<T, CacheT, QT, 4 * V>);
+    case 8: return go(prepass_vec_kernel<T, CacheT, QT, 8 * V>);
+    case 16: return go(prepass_vec_kernel<T, CacheT, QT, 16 * V>);
+    case 32: return go(prepass_vec_kernel<T, CacheT, QT, 32 * V>);
     default: return cudaSuccess;  // not a power-of-two chunk count: the generic kernel runs
   }
 }
