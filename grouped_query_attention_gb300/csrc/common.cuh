@@ -43,6 +43,13 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return *reinterpret_cast<float2*>(&dv);
 }
 
+// Maximum of three values (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Rotary table row element (T) as fp32.
 __device__ __forceinline__ float rot_t(const void* base, long long idx, int t_type) {
   return load_t(base, idx, t_type);

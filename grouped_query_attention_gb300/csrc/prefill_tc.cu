@@ -349,7 +349,8 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
         float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
         if (full) {
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) m4[e & 3] = fmaxf(m4[e & 3], __uint_as_float(r[e]));
+          for (int e = 0; e < kBN; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
         } else {
 #pragma unroll
           for (int e = 0; e < kBN; ++e)
@@ -405,6 +406,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       // Pass 2: P = exp2(score - m) as fp16 pairs over the first 64 columns of
       // S_q, 64 scores per load batch; columns are overwritten only after read.
       const float neg_m = -m_run;
+      const float2 scale2 = make_float2(qk_scale, qk_scale), negm2 = make_float2(neg_m, neg_m);
       float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -419,8 +421,9 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           const float xa = __uint_as_float(r[2 * k]), xb = __uint_as_float(r[2 * k + 1]);
           float pa, pb;
           if constexpr (PLAIN) {
-            pa = ex2(fmaf(xa, qk_scale, neg_m));
-            pb = ex2(fmaf(xb, qk_scale, neg_m));
+            const float2 arg = ffma2(make_float2(xa, xb), scale2, negm2);
+            pa = ex2(arg.x);
+            pb = ex2(arg.y);
             if (!full) {
               pa = (col >= lo && col < hi) ? pa : 0.f;
               pb = (col + 1 >= lo && col + 1 < hi) ? pb : 0.f;
