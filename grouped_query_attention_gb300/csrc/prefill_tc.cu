@@ -347,15 +347,18 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
         for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, r + c * 32);
         tmem_ld_wait();
         float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
-        if (full) {
+        if (!full) {
+          // Masked columns become -inf in tensor memory too, so pass 2 needs
+          // no mask (the scale is positive: exp2 of -inf * scale - m is 0).
 #pragma unroll
-          for (int e = 0; e < kBN; e += 2)
-            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-        } else {
+          for (int e = 0; e < kBN; ++e) r[e] = (e >= lo && e < hi) ? r[e] : 0xff800000u;
 #pragma unroll
-          for (int e = 0; e < kBN; ++e)
-            m4[e & 3] = (e >= lo && e < hi) ? fmaxf(m4[e & 3], __uint_as_float(r[e])) : m4[e & 3];
+          for (int c = 0; c < 4; ++c) tmem_st32(s_addr + c * 32, r + c * 32);
+          tmem_st_wait();
         }
+#pragma unroll
+        for (int e = 0; e < kBN; e += 2)
+          m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
         const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         mt = m > kNegBig ? m * qk_scale : kNegBig;
       } else {
@@ -417,17 +420,12 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
         uint32_t packed[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int col = hf * 64 + 2 * k;
           const float xa = __uint_as_float(r[2 * k]), xb = __uint_as_float(r[2 * k + 1]);
           float pa, pb;
           if constexpr (PLAIN) {
             const float2 arg = ffma2(make_float2(xa, xb), scale2, negm2);
             pa = ex2(arg.x);
             pb = ex2(arg.y);
-            if (!full) {
-              pa = (col >= lo && col < hi) ? pa : 0.f;
-              pb = (col + 1 >= lo && col + 1 < hi) ? pb : 0.f;
-            }
           } else {
             pa = xa <= kNegBig ? 0.f : ex2(xa + neg_m);
             pb = xb <= kNegBig ? 0.f : ex2(xb + neg_m);
@@ -508,7 +506,8 @@ bool g_smem_set[2][kMaxDevices];
 
 cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& maps) {
   const int smem = (int)sizeof(TcSmem) + 1024;
-  const bool plain = p.softcap <= 0.f && !p.has_bias;
+  // The plain kernel scales the row max once, which needs a positive scale.
+  const bool plain = p.softcap <= 0.f && !p.has_bias && p.scale > 0.f;
   auto kern = plain ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
