@@ -376,7 +376,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             for (int e = 0; e < 32; ++e) {
               const int col = hf * 64 + c + e;
               const float x = score(__uint_as_float(r[c + e]), bv[e], qk_scale, p.softcap, inv_cap);
-              const float y = (full || (col >= lo && col < hi)) ? x : kNegBig;
+              const float y = (full || (col >= lo && col < hi)) ? x : -INFINITY;
               mt = fmaxf(mt, y);
               r[c + e] = __float_as_uint(y);
             }
@@ -426,9 +426,10 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             const float2 arg = ffma2(make_float2(xa, xb), scale2, negm2);
             pa = ex2(arg.x);
             pb = ex2(arg.y);
-          } else {
-            pa = xa <= kNegBig ? 0.f : ex2(xa + neg_m);
-            pb = xb <= kNegBig ? 0.f : ex2(xb + neg_m);
+          } else {   // masked scores are -inf: exp2 gives 0
+            const float2 arg = ffma2(make_float2(xa, xb), make_float2(1.f, 1.f), negm2);
+            pa = ex2(arg.x);
+            pb = ex2(arg.y);
           }
           ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
           const __half2 hp = __floats2half2_rn(pa, pb);
