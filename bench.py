@@ -274,7 +274,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     plan = op.plan(**call)
     ws = torch.empty(max(int(plan.workspace_bytes), 256), dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    flush_words = flush.view(torch.int32)
+    flush_words = flush.view(torch.float32)   # summed in place (no widening copy)
 
     def flush_l2():
         # Write a buffer larger than L2, then read it back, so that the timed
@@ -355,7 +355,8 @@ def run_gpu_arm(args, world, rank, local) -> None:
     e2e_value = units_all / (e2e_ms / 1e3)
 
     peaks, peaks_src = load_peaks()
-    kernel_src = {"decode": ["decode.cu"], "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
+    kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": ["decode_tc.cu", "tcgen05.cuh"],
+                  "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
                   "copy_past": ["prepass.cu"]}[dominant]
     if wk["bound"] == "hbm":

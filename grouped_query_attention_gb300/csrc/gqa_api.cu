@@ -446,7 +446,7 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
   if (pl.decode) {
-    e = timed_launch(h, GQA_KERNEL_DECODE, st,
+    e = timed_launch(h, pl.tc_decode ? GQA_KERNEL_DECODE_TENSOR_CORE : GQA_KERNEL_DECODE, st,
                      [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st, maps) : gqa::launch_decode(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   } else {
@@ -485,7 +485,7 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
-  e = timed_launch(h, GQA_KERNEL_DECODE, st,
+  e = timed_launch(h, pl.tc_decode ? GQA_KERNEL_DECODE_TENSOR_CORE : GQA_KERNEL_DECODE, st,
                    [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st, maps) : gqa::launch_decode(P, st); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return GQA_OK;

@@ -177,9 +177,9 @@ GQA_API gqa_status gqa_forward(gqa_handle* handle, const gqa_inputs* in, const g
  *     fixed array of 16 MiB compiled into the library; every GPU that loads
  *     the library holds it until the process exits. Nothing is allocated:
  *     no cudaMalloc, cudaFree or allocating library routine is called.
- *   - Only the decode regime (S * num_heads / kv_num_heads <= 8, head size 64
- *     or 128); other calls return GQA_ERR_UNSUPPORTED. A call that needs more
- *     than 16 MiB of scratch returns GQA_ERR_WORKSPACE with the size it needs.
+ *   - Only the decode regime (gqa_describe_plan reports GQA_REGIME_DECODE);
+ *     other calls return GQA_ERR_UNSUPPORTED. A call that needs more than
+ *     16 MiB of scratch returns GQA_ERR_WORKSPACE with the size it needs.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -205,7 +205,12 @@ GQA_API gqa_status gqa_read_device_status(gqa_handle* handle, void* workspace, v
  * (GQA_REGIME_DECODE: one fused split-KV launch; GQA_REGIME_PREFILL: pre-pass
  * then flash prefill), the number of kernel launches per call, the decode
  * split length / split count (0 for prefill) and the workspace bytes. Same
- * checks and status codes as gqa_workspace_size. */
+ * checks and status codes as gqa_workspace_size.
+ * Decode regime: up to 8 query rows per KV head (S * num_heads / kv_num_heads)
+ * with head size 64 or 128 on the CUDA-core kernel (split_len = keys per
+ * split, max_splits = splits per (batch, KV head)), or, for fp16 inputs and
+ * cache with head size 128, up to 16 rows on the tensor-core kernel
+ * (split_len = 128 keys per work unit, max_splits = partial-result slots). */
 #define GQA_REGIME_DECODE 1
 #define GQA_REGIME_PREFILL 2
 typedef struct gqa_plan_info {
@@ -231,6 +236,7 @@ GQA_API gqa_status gqa_describe_plan(const gqa_handle* handle, const gqa_inputs*
 #define GQA_KERNEL_DECODE 3
 #define GQA_KERNEL_PREFILL_CUDA_CORE 4
 #define GQA_KERNEL_PREFILL_TENSOR_CORE 5
+#define GQA_KERNEL_DECODE_TENSOR_CORE 6
 GQA_API gqa_status gqa_profile_begin(gqa_handle* handle, int32_t max_launches);
 GQA_API gqa_status gqa_profile_end(gqa_handle* handle, int32_t* kinds, float* ms, int32_t capacity, int32_t* count);
 
