@@ -240,118 +240,150 @@ __device__ void map_segment(const Params& p, long long t, long long tend, long l
   it.end = 1;   // not reached for t < ntot
 }
 
-// Row of H values held as x[e] = element lane + 32e: RMS norm then NeoX rotary
-// (the rotary partner of element e is e +- 2, in the same lane).
-__device__ __forceinline__ void norm_rope(const Params& p, float* x, const void* w, int pos, bool norm, bool rope) {
-  const int lane = threadIdx.x & 31;
+// Rows of H = 128 fp16 values, eight lanes per row and four rows per warp
+// pass: lane part l8 = lane & 7 holds dims 8*l8 .. 8*l8+7 (lo) and
+// 64+8*l8 .. 64+8*l8+7 (hi), so the NeoX rotary partner of every value is in
+// the same lane and each half is one 16-byte chunk.
+__device__ __forceinline__ void h8_to_f(const uint4& u, float* f) {
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 v = __half22float2(h[k]);
+    f[2 * k] = v.x;
+    f[2 * k + 1] = v.y;
+  }
+}
+
+__device__ __forceinline__ uint4 f_to_h8(const float* f, float scale) {
+  uint4 u;
+  __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(f[2 * k] * scale, f[2 * k + 1] * scale);
+  return u;
+}
+
+// RMS norm (weights w, or none) then rotary (cos / sin of the row's position,
+// or none) of one row held as lo / hi halves; the row's 8 lanes reduce together.
+__device__ __forceinline__ void norm_rope8(const Params& p, float* lo, float* hi, const float* wlo, const float* whi,
+                                           bool norm, const uint4* cs, const uint4* sn) {
   if (norm) {
     float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) ss += x[e] * x[e];
+    for (int k = 0; k < 8; ++k) ss += lo[k] * lo[k] + hi[k] * hi[k];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float rn = 1.0f / sqrtf(ss / (float)kHD + p.eps);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = (x[e] * rn) * load_t(w, lane + 32 * e, p.t_type);
-  }
-  if (rope) {
-    float y[4];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int dc = lane + 32 * e;
-      const float cs = load_t(p.cos_c, (long long)pos * (kHD / 2) + dc, p.t_type);
-      const float sn = load_t(p.sin_c, (long long)pos * (kHD / 2) + dc, p.t_type);
-      y[e] = x[e] * cs - x[e + 2] * sn;
-      y[e + 2] = x[e + 2] * cs + x[e] * sn;
+    for (int k = 0; k < 8; ++k) {
+      lo[k] = (lo[k] * rn) * wlo[k];
+      hi[k] = (hi[k] * rn) * whi[k];
     }
+  }
+  if (cs) {
+    float c[8], sv[8];
+    h8_to_f(*cs, c);
+    h8_to_f(*sn, sv);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = y[e];
+    for (int k = 0; k < 8; ++k) {
+      const float a = lo[k], b = hi[k];
+      lo[k] = a * c[k] - b * sv[k];
+      hi[k] = b * c[k] + a * sv[k];
+    }
   }
 }
 
 // The group's query rows of an item as fp16 MMA operand rows (scaled into the
-// log2 domain unless softcap). Rows >= R stay zero from the kernel start. All
-// loads are issued before the arithmetic, so their latencies overlap.
-template <int R>
+// log2 domain unless softcap). Rows >= R stay zero from the kernel start.
 __device__ void prepare_qt(const Params& p, const DItem& it, uint8_t* qt) {
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, l8 = lane & 7, sub = lane >> 3;
   const int rows = p.S * p.G;
   const float qscale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
   const __half* q = reinterpret_cast<const __half*>(p.q);
-  const __half* cosc = reinterpret_cast<const __half*>(p.cos_c);
-  const __half* sinc = reinterpret_cast<const __half*>(p.sin_c);
-  float x[R][4], cs[R][2], sn[R][2], w[4];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (r >= rows) continue;
-    const int i = r / p.G, h = it.g * p.G + r % p.G;
-    const long long src = ((long long)(it.b * p.S + i) * p.N + h) * kHD;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) x[r][e] = __half2float(q[src + lane + 32 * e]);
-    if (p.has_rotary) {
-      const long long cbase = (long long)(it.past + i) * (kHD / 2);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        cs[r][e] = __half2float(cosc[cbase + lane + 32 * e]);
-        sn[r][e] = __half2float(sinc[cbase + lane + 32 * e]);
-      }
-    }
+  float wlo[8], whi[8];
+  if (p.has_norm) {
+    const __half* w = reinterpret_cast<const __half*>(p.qw);
+    h8_to_f(*reinterpret_cast<const uint4*>(w + 8 * l8), wlo);
+    h8_to_f(*reinterpret_cast<const uint4*>(w + 64 + 8 * l8), whi);
   }
-#pragma unroll
-  for (int e = 0; e < 4; ++e)
-    w[e] = p.has_norm ? __half2float(reinterpret_cast<const __half*>(p.qw)[lane + 32 * e]) : 1.f;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (r >= rows) continue;
-    float* v = x[r];
-    if (p.has_norm) {
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) ss += v[e] * v[e];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float rn = 1.0f / sqrtf(ss / (float)kHD + p.eps);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = (v[e] * rn) * w[e];
-    }
+#pragma unroll 1
+  for (int r0 = 0; r0 < rows; r0 += 4) {
+    const int r = min(r0 + sub, rows - 1);   // lanes past the last row redo it and do not store
+    const int i = r / p.G, h = it.g * p.G + r % p.G;
+    const __half* src = q + ((long long)(it.b * p.S + i) * p.N + h) * kHD;
+    const uint4 xl = *reinterpret_cast<const uint4*>(src + 8 * l8);
+    const uint4 xh = *reinterpret_cast<const uint4*>(src + 64 + 8 * l8);
+    uint4 cs, sn;
     if (p.has_rotary) {
-      float y[4];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        y[e] = v[e] * cs[r][e] - v[e + 2] * sn[r][e];
-        y[e + 2] = v[e + 2] * cs[r][e] + v[e] * sn[r][e];
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = y[e];
+      const long long cb = (long long)(it.past + i) * (kHD / 2) + 8 * l8;
+      cs = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.cos_c) + cb);
+      sn = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.sin_c) + cb);
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      *reinterpret_cast<__half*>(qt + sw_elem(r, lane + 32 * e, kRowBox)) = __float2half_rn(v[e] * qscale);
+    float lo[8], hi[8];
+    h8_to_f(xl, lo);
+    h8_to_f(xh, hi);
+    norm_rope8(p, lo, hi, wlo, whi, p.has_norm, p.has_rotary ? &cs : nullptr, &sn);
+    if (r0 + sub < rows) {
+      *reinterpret_cast<uint4*>(qt + sw128_offset(r, l8)) = f_to_h8(lo, qscale);
+      *reinterpret_cast<uint4*>(qt + kRowBox + sw128_offset(r, l8)) = f_to_h8(hi, qscale);
+    }
   }
 }
 
 // Append the new rows of (b, g) that fall in the segment's keys to the
-// present cache (K: norm, rotary; cast to fp16). Prompt padding rows (past the
-// total length) go with the segment that holds the last tile.
+// present cache (K: norm, rotary; V: as given; fp16). Prompt padding rows
+// (past the total length) go with the segment that holds the last tile. One
+// pass handles four (row, K or V) pairs.
 __device__ void append_rows(const Params& p, const DItem& it) {
-  const int lane = threadIdx.x & 31;
-  for (int i = 0; i < p.S; ++i) {
-    const int j = it.past + i;
-    const bool mine = j < it.total ? (j >= it.j0 && j < it.jend) : it.last != 0;
-    if (!mine) continue;
+  const int lane = threadIdx.x & 31, l8 = lane & 7, sub = lane >> 3;
+  float wlo[8], whi[8];
+  if (p.has_norm) {
+    const __half* w = reinterpret_cast<const __half*>(p.kw);
+    h8_to_f(*reinterpret_cast<const uint4*>(w + 8 * l8), wlo);
+    h8_to_f(*reinterpret_cast<const uint4*>(w + 64 + 8 * l8), whi);
+  }
+  const int n = 2 * p.S;   // pair x: row i = x / 2, K for even x, V for odd x
+#pragma unroll 1
+  for (int x0 = 0; x0 < n; x0 += 4) {
+    const int x = min(x0 + sub, n - 1);
+    const int i = x >> 1, j = it.past + i;
+    const bool is_k = (x & 1) == 0;
+    const bool mine = (x0 + sub < n) && (j < it.total ? (j >= it.j0 && j < it.jend) : it.last != 0);
     const long long src = ((long long)(it.b * p.S + i) * p.Nkv + it.g) * kHD;
-    const long long dst = (((long long)it.b * p.Nkv + it.g) * p.C + j) * kHD;
-    float x[4], v[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[e] = load_t(p.k, src + lane + 32 * e, p.t_type);
-      v[e] = load_t(p.v, src + lane + 32 * e, p.t_type);
+    const __half* base = reinterpret_cast<const __half*>(is_k ? p.k : p.v) + src;
+    const uint4 xl = *reinterpret_cast<const uint4*>(base + 8 * l8);
+    const uint4 xh = *reinterpret_cast<const uint4*>(base + 64 + 8 * l8);
+    uint4 cs, sn;
+    const bool rope = is_k && p.has_rotary;
+    if (rope) {
+      const long long cb = (long long)j * (kHD / 2) + 8 * l8;
+      cs = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.cos_c) + cb);
+      sn = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.sin_c) + cb);
     }
-    norm_rope(p, x, p.kw, j, p.has_norm, p.has_rotary);
+    float lo[8], hi[8];
+    h8_to_f(xl, lo);
+    h8_to_f(xh, hi);
+    // K and V rows of a pass may sit in one 8-lane group's neighbours: every
+    // lane takes part in the norm's shuffles; V rows ignore the result.
+    float klo[8], khi[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      reinterpret_cast<__half*>(p.present_k)[dst + lane + 32 * e] = __float2half_rn(x[e]);
-      reinterpret_cast<__half*>(p.present_v)[dst + lane + 32 * e] = __float2half_rn(v[e]);
+    for (int k = 0; k < 8; ++k) {
+      klo[k] = lo[k];
+      khi[k] = hi[k];
+    }
+    norm_rope8(p, klo, khi, wlo, whi, p.has_norm, nullptr, nullptr);
+    if (is_k && p.has_norm) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        lo[k] = klo[k];
+        hi[k] = khi[k];
+      }
+    }
+    if (rope) norm_rope8(p, lo, hi, wlo, whi, false, &cs, &sn);
+    if (mine) {
+      __half* dst = reinterpret_cast<__half*>(is_k ? p.present_k : p.present_v) +
+                    (((long long)it.b * p.Nkv + it.g) * p.C + j) * kHD;
+      *reinterpret_cast<uint4*>(dst + 8 * l8) = f_to_h8(lo, 1.f);
+      *reinterpret_cast<uint4*>(dst + 64 + 8 * l8) = f_to_h8(hi, 1.f);
     }
   }
 }
@@ -470,7 +502,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         sm.item[slot] = it;
         mbar_arrive(&sm.imap[slot]);
       }
-      prepare_qt<R>(p, it, sm.qt[slot]);
+      prepare_qt(p, it, sm.qt[slot]);
       append_rows(p, it);
       fence_async_all();  // query rows (shared) and appended rows (global) -> async proxy
       __syncwarp();
