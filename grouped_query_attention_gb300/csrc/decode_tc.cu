@@ -412,7 +412,7 @@ __device__ __forceinline__ void write_out(const Params& p, int b, int g, int tot
 
 // ---------------------------------------------------------------- the kernel
 
-template <int R>
+template <int R, bool kPlain>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ uint8_t smem_raw[];
@@ -695,8 +695,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
             bool vis = key_ok && ih_r[r] >= 0;
             if (p.causal) vis = vis && jk <= pos_r[r];
             if (p.window >= 0) vis = vis && jk >= pos_r[r] - p.window;
-            if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap) * kLog2e;
-            if (p.has_bias && vis) {
+            if (!kPlain && p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap) * kLog2e;
+            if (!kPlain && p.has_bias && vis) {
               const int i = ih_r[r] / p.N, h = ih_r[r] % p.N;
               const long long bi =
                   (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
@@ -860,17 +860,17 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
 // (racing first calls store the same values).
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];
-bool g_smem_set[5][kMaxDevices];
+bool g_smem_set[10][kMaxDevices];
 
-template <int R>
-cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv, int ri) {
+template <int R, bool kPlain>
+cudaError_t launch_rp(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv, int ri) {
   const int smem = (int)sizeof(DSmem) + 1024;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!g_smem_set[ri][dev]) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_tc_kernel<R, kPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     g_smem_set[ri][dev] = true;
   }
@@ -881,8 +881,16 @@ cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, co
   }
   const int sms = g_sm_count[dev];
   const int grid = sms < kTcDecodeMaxCtas ? sms : kTcDecodeMaxCtas;
-  decode_tc_kernel<R><<<grid, kThreads, smem, st>>>(p, mk, mv);
+  decode_tc_kernel<R, kPlain><<<grid, kThreads, smem, st>>>(p, mk, mv);
   return cudaGetLastError();
+}
+
+// Scores without softcap or bias take a kernel whose tile loop has no code
+// for them.
+template <int R>
+cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv, int ri) {
+  if (p.softcap > 0.f || p.has_bias) return launch_rp<R, false>(p, st, mk, mv, ri);
+  return launch_rp<R, true>(p, st, mk, mv, ri + 5);
 }
 
 }  // namespace
