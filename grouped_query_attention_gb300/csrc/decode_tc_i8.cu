@@ -1,0 +1,1024 @@
+// Tensor-core split-KV decode for an int8 cache with fp32 queries and output
+// (head size 128, at most 8 query rows per KV head), sm_103a.
+//
+// Same structure as the fp16 tensor-core decode (balanced shares of 128-key
+// tiles over persistent CTAs, S^T = K Q^T and O^T += V^T P^T per tile in
+// tensor memory, one softmax thread per key), with two additions:
+//   - int8 codes are exact in fp16, so TMA brings the int8 K / V tiles and
+//     four converter warps (7..10) rewrite them as fp16 MMA operand tiles;
+//   - fp32 accuracy: each prepared query row q' (norm, rotary, scale, K
+//     channel scale folded in, times a power of two 2^-e that brings its
+//     largest value to [1, 2)) is split into two fp16 rows hi = fp16(q'),
+//     lo = fp16(q' - hi), placed as MMA rows r and r+R; the products with the
+//     codes are exact and accumulate in fp32, so S = (S_hi + S_lo) 2^e holds
+//     q' to about 2^-22. Probabilities are split the same way for P.V, and
+//     the V channel scale multiplies O once at the end.
+// Warp roles: 0 TMA (int8 tiles, 3 stages each for K and V), 1 MMA, 2
+// preparer (segments, query rows, appended int8 rows), 3..6 softmax, 7..10
+// converters (K into one of two fp16 buffers, V into one).
+//
+// com.microsoft.GroupQueryAttention, section Implementation variants
+// (quant_int8_decode_splitk: int8 rows appended with k/v_scale, attention over
+// the stored codes times the scales, split-K with a merge of partial results)
+// and sections Inputs (k_scale, v_scale) / Attributes (k/v_quant_type).
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "tcgen05.cuh"
+#include "tma_host.h"
+
+namespace gqa {
+namespace {
+
+using namespace tc;
+
+constexpr int kHD = 128;
+constexpr int kKT = kTcDecodeTile;       // keys per tile (128)
+constexpr int kNR = 16;                  // MMA N: hi and lo query rows of the group, padded
+constexpr int kNS = 3;                   // int8 K stages
+constexpr int kNSV = 2;                  // int8 V stages
+constexpr int kThreads = 352;            // TMA, MMA, preparer, 4 softmax, 4 converter warps
+constexpr int kSoftWarp0 = 3;            // first softmax warp
+constexpr int kConvWarp0 = 7;            // first converter warp
+constexpr int kSoft = 128;               // softmax threads
+constexpr int kConv = 128;               // converter threads
+constexpr uint32_t kBox = 128u * 128u;   // 64 columns x 128 rows (fp16) = 16 KB
+constexpr uint32_t kTile = 2u * kBox;    // fp16 K or V tile: 128 keys x 128 dims
+constexpr uint32_t kTile8 = 128u * 128u; // int8 K or V tile: 128 keys x 128 dims
+constexpr uint32_t kRowBox = 16u * 128u; // 64 columns x 16 rows = 2 KB
+constexpr float kLazy = 8.0f;            // log2 growth tolerated before rescaling O
+constexpr uint32_t kIdS = idesc_f16(128, kNR, 0, 0);   // K (K-major) x Q^T rows (K-major)
+constexpr uint32_t kIdO = idesc_f16(128, kNR, 1, 0);   // V (MN-major) x P^T rows (K-major)
+// Tensor memory: S^T buffers at columns 0 and 16, O^T at 32 (16 columns each).
+
+struct DItem {
+  int b, g;
+  int split, nsplit;     // this segment's index among the CTAs sharing (b, g), their count
+  int slot, slot0;       // partial slot of this segment / of the first segment of (b, g)
+  int cfirst;            // first CTA of (b, g)
+  int j0, jend;          // keys of this segment: [j0, jend)
+  int last;              // the segment holds the last tile of (b, g)
+  int past, total, ntiles, end;
+};
+
+struct __align__(1024) DSmem {
+  uint8_t k8[kNS][kTile8];      // int8 tiles as loaded (128-byte swizzle)
+  uint8_t v8[kNSV][kTile8];
+  uint8_t k[2][kTile];          // fp16 K operand tiles (two buffers)
+  uint8_t v[2][kTile];          // fp16 V operand tiles (two buffers)
+  uint8_t qt[2][2 * kRowBox];   // per item slot: hi / lo query rows (16 x 128, fp16, swizzled)
+  uint8_t pt[2][2 * kRowBox];   // P^T buffers: hi / lo rows x 128 keys (fp16, swizzled)
+  float red[2][4][kNR];         // cross-warp row max, double-buffered by tile parity
+  float redl[4][kNR];           // cross-warp row sum
+  float qpow[2][8];             // per item slot: 2^e of each query row
+  DItem item[2];
+  uint64_t kfull[kNS], kempty[kNS], vfull[kNSV], vempty[kNSV];   // int8 stages
+  uint64_t k16full[2], k16empty[2], v16full[2], v16empty[2];      // fp16 operand tiles
+  uint64_t imap[2], iready[2], iempty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort;
+  int last;
+};
+
+__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory"); }
+
+// Merge ticket with acquire-release ordering at GPU scope: after the named
+// barrier, the release covers every softmax thread's partial stores, and the
+// acquire makes the other splits' partials visible to the last one.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* addr) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(addr) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+__device__ __forceinline__ bool aborted(const DSmem& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
+}
+
+__device__ __forceinline__ void set_abort(const Params& p, DSmem& sm) {
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+  flag_status(p, GQA_DEVICE_TIMEOUT_BIT);
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Byte offset of element (row, col) in a [rows][128] fp16 matrix stored as two
+// 64-column boxes of `box` bytes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_elem(uint32_t row, uint32_t col, uint32_t box) {
+  return (col >> 6) * box + sw128_offset(row, (col & 63) >> 3) + (col & 7) * 2;
+}
+
+// ---------------------------------------------------------------- producer helpers
+
+// Tiles of batch b (its key range [kstart, total) in 128-key tiles, for each
+// KV head); 0 for a batch whose lengths are inconsistent.
+__device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, int& total, bool flag_bad) {
+  total = p.seqlens[b] + 1;
+  past = batch_past(p, total);
+  if (past >= 0 && p.has_rotary && past + p.S > p.rotary_rows) {
+    if (flag_bad) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
+    past = -1;
+  } else if (past < 0 && flag_bad) {
+    flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
+  }
+  if (past < 0) return 0;
+  const int kstart = p.window >= 0 ? max(0, past - p.window) : 0;
+  return (total - kstart + kKT - 1) / kKT;
+}
+
+// Work units of a (b, g) with `tiles` tiles: one per tile plus kEndUnits for
+// the end of its key range (the epilogue that writes the output or a partial
+// costs about as much as that many tiles). Shares are equal in units, so a
+// CTA that ends more key ranges gets fewer tiles.
+constexpr int kEndUnits = 5;
+__device__ __forceinline__ long long bg_units(int tiles) { return tiles > 0 ? tiles + kEndUnits : 0; }
+
+// Number of work units over all (b, g) (whole warp).
+__device__ long long count_units(const Params& p, bool flag_bad) {
+  const int lane = threadIdx.x & 31;
+  long long n = 0;
+  for (int b = lane; b < p.B; b += 32) {
+    int past, total;
+    n += bg_units(batch_tiles(p, b, past, total, flag_bad)) * p.Nkv;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+  return n;
+}
+
+// CTA owning global unit t when `ntot` units are shared by `nc` <= ntot CTAs
+// (CTA c owns [c*ntot/nc, (c+1)*ntot/nc), never empty).
+__device__ __forceinline__ long long share_start(long long c, long long ntot, long long nc) { return c * ntot / nc; }
+__device__ __forceinline__ int tile_owner(long long t, long long ntot, long long nc) {
+  return (int)(((t + 1) * nc - 1) / ntot);
+}
+
+// The segment that starts at global unit t and ends at min(tend, last tile of
+// its (b, g)), with a warp-wide prefix scan of the per-batch unit counts. A
+// unit past the last tile of its (b, g) gives end = 2 and, in ntiles, the
+// units to skip to the next (b, g).
+__device__ void map_segment(const Params& p, long long t, long long tend, long long ntot, long long nc,
+                            DItem& it) {
+  const int lane = threadIdx.x & 31;
+  long long base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    int past = -1, total = 0, tb = 0;
+    if (b < p.B) tb = batch_tiles(p, b, past, total, false);
+    const long long n = bg_units(tb) * p.Nkv;
+    long long incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long excl = base + incl - n;
+    const unsigned ballot = __ballot_sync(0xffffffffu, n > 0 && t >= excl && t < excl + n);
+    if (ballot) {
+      const int src = __ffs(ballot) - 1;
+      const int pp = __shfl_sync(0xffffffffu, past, src);
+      const int tt = __shfl_sync(0xffffffffu, total, src);
+      const int tiles = __shfl_sync(0xffffffffu, tb, src);
+      const long long r = t - __shfl_sync(0xffffffffu, excl, src);
+      const int blk = (int)bg_units(tiles);
+      it.b = __shfl_sync(0xffffffffu, b, src);
+      it.g = (int)(r / blk);
+      const int lt = (int)(r % blk);
+      if (lt >= tiles) {   // end units of the (b, g): nothing to load
+        it.end = 2;
+        it.ntiles = blk - lt;
+        return;
+      }
+      const long long first = t - lt, bg_end = first + tiles;
+      const long long seg_end = tend < bg_end ? tend : bg_end;
+      const int kstart = p.window >= 0 ? max(0, pp - p.window) : 0;
+      it.past = pp;
+      it.total = tt;
+      it.j0 = kstart + lt * kKT;
+      it.jend = min(tt, kstart + (int)(seg_end - first) * kKT);
+      it.ntiles = (int)(seg_end - t);
+      it.last = seg_end == bg_end;
+      it.cfirst = tile_owner(first, ntot, nc);
+      it.nsplit = tile_owner(bg_end - 1, ntot, nc) - it.cfirst + 1;
+      it.split = (int)blockIdx.x - it.cfirst;
+      it.slot0 = 2 * it.cfirst + (share_start(it.cfirst, ntot, nc) != first ? 1 : 0);
+      it.slot = it.split == 0 ? it.slot0 : 2 * (int)blockIdx.x;
+      it.end = 0;
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  it.end = 1;   // not reached for t < ntot
+}
+
+// Rows of H = 128 values, eight lanes per row and four rows per warp pass:
+// lane part l8 = lane & 7 holds dims 8*l8 .. 8*l8+7 (lo) and 64+8*l8 ..
+// 64+8*l8+7 (hi), so the NeoX rotary partner of every value is in the same
+// lane.
+__device__ __forceinline__ void load8f(const float* src, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 c = *reinterpret_cast<const float4*>(src + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
+}
+
+__device__ __forceinline__ uint4 f_to_h8(const float* f) {
+  uint4 u;
+  __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+  return u;
+}
+
+// RMS norm (weights w) and / or rotary (cos c, sin s) of one row held as lo /
+// hi halves; the row's 8 lanes reduce together (every lane must call).
+__device__ __forceinline__ void norm_rope8(const Params& p, float* lo, float* hi, const float* wlo, const float* whi,
+                                           bool norm, bool rope, const float* c, const float* sv) {
+  if (norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss += lo[k] * lo[k] + hi[k] * hi[k];
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rn = 1.0f / sqrtf(ss / (float)kHD + p.eps);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo[k] = (lo[k] * rn) * wlo[k];
+      hi[k] = (hi[k] * rn) * whi[k];
+    }
+  }
+  if (rope) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float a = lo[k], b = hi[k];
+      lo[k] = a * c[k] - b * sv[k];
+      hi[k] = b * c[k] + a * sv[k];
+    }
+  }
+}
+
+// The group's query rows of an item: q' = rotary(norm(q)) * scale (log2
+// domain unless softcap) * K channel scale, times 2^-e with 2^e the power of
+// two at or below the row's largest |q'|; hi = fp16(q' 2^-e) goes to MMA row
+// r, lo = fp16(q' 2^-e - hi) to row r + R. Rows >= 2R stay zero.
+__device__ void prepare_qt(const Params& p, const DItem& it, int R, uint8_t* qt, float* qpow) {
+  const int lane = threadIdx.x & 31, l8 = lane & 7, sub = lane >> 3;
+  const int rows = p.S * p.G;
+  const float qscale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
+  const float* q = reinterpret_cast<const float*>(p.q);
+  float wlo[8], whi[8], kslo[8], kshi[8];
+  if (p.has_norm) {
+    load8f(reinterpret_cast<const float*>(p.qw) + 8 * l8, wlo);
+    load8f(reinterpret_cast<const float*>(p.qw) + 64 + 8 * l8, whi);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    kslo[k] = channel_scale(p.k_scale, p.k_scale_n, it.g * kHD + 8 * l8 + k);
+    kshi[k] = channel_scale(p.k_scale, p.k_scale_n, it.g * kHD + 64 + 8 * l8 + k);
+  }
+#pragma unroll 1
+  for (int r0 = 0; r0 < rows; r0 += 4) {
+    const int r = min(r0 + sub, rows - 1);   // lanes past the last row redo it and do not store
+    const int i = r / p.G, h = it.g * p.G + r % p.G;
+    const float* src = q + ((long long)(it.b * p.S + i) * p.N + h) * kHD;
+    float lo[8], hi[8], c[8], sv[8];
+    load8f(src + 8 * l8, lo);
+    load8f(src + 64 + 8 * l8, hi);
+    if (p.has_rotary) {
+      const long long cb = (long long)(it.past + i) * (kHD / 2) + 8 * l8;
+      load8f(reinterpret_cast<const float*>(p.cos_c) + cb, c);
+      load8f(reinterpret_cast<const float*>(p.sin_c) + cb, sv);
+    }
+    norm_rope8(p, lo, hi, wlo, whi, p.has_norm, p.has_rotary, c, sv);
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo[k] = lo[k] * qscale * kslo[k];
+      hi[k] = hi[k] * qscale * kshi[k];
+      mx = fmaxf(mx, fmaxf(fabsf(lo[k]), fabsf(hi[k])));
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // 2^e <= mx < 2^(e+1) from the exponent bits (mx = 0 or subnormal: e = 0).
+    const int ebits = (__float_as_int(mx) >> 23) & 0xff;
+    const int e = ebits == 0 ? 0 : ebits - 127;
+    const float down = __int_as_float((127 - e) << 23), up = __int_as_float((127 + e) << 23);
+    float hl[8], hh[8], ll[8], lh[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float a = lo[k] * down, b = hi[k] * down;
+      hl[k] = __half2float(__float2half_rn(a));
+      hh[k] = __half2float(__float2half_rn(b));
+      ll[k] = a - hl[k];
+      lh[k] = b - hh[k];
+    }
+    if (r0 + sub < rows) {
+      *reinterpret_cast<uint4*>(qt + sw128_offset(r, l8)) = f_to_h8(hl);
+      *reinterpret_cast<uint4*>(qt + kRowBox + sw128_offset(r, l8)) = f_to_h8(hh);
+      *reinterpret_cast<uint4*>(qt + sw128_offset(r + R, l8)) = f_to_h8(ll);
+      *reinterpret_cast<uint4*>(qt + kRowBox + sw128_offset(r + R, l8)) = f_to_h8(lh);
+      if (l8 == 0) qpow[r] = up;
+    }
+  }
+}
+
+// Eight int8 codes (clamp(rint(x / scale), -127, 127), IEEE division) as one 8-byte word.
+__device__ __forceinline__ uint2 quant8(const float* x, const float* sc) {
+  uint2 u;
+  int8_t* b = reinterpret_cast<int8_t*>(&u);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) b[k] = quant_i8(x[k], sc[k]);
+  return u;
+}
+
+// Append the new rows of (b, g) that fall in the segment's keys to the
+// present cache as int8 codes (K: norm, rotary, then k_scale; V: v_scale).
+// Prompt padding rows (past the total length) go with the segment that holds
+// the last tile. One pass handles four (row, K or V) pairs.
+__device__ void append_rows(const Params& p, const DItem& it) {
+  const int lane = threadIdx.x & 31, l8 = lane & 7, sub = lane >> 3;
+  float wlo[8], whi[8];
+  if (p.has_norm) {
+    load8f(reinterpret_cast<const float*>(p.kw) + 8 * l8, wlo);
+    load8f(reinterpret_cast<const float*>(p.kw) + 64 + 8 * l8, whi);
+  }
+  const int n = 2 * p.S;   // pair x: row i = x / 2, K for even x, V for odd x
+#pragma unroll 1
+  for (int x0 = 0; x0 < n; x0 += 4) {
+    const int x = min(x0 + sub, n - 1);
+    const int i = x >> 1, j = it.past + i;
+    const bool is_k = (x & 1) == 0;
+    const bool mine = (x0 + sub < n) && (j < it.total ? (j >= it.j0 && j < it.jend) : it.last != 0);
+    const float* base = reinterpret_cast<const float*>(is_k ? p.k : p.v) +
+                        ((long long)(it.b * p.S + i) * p.Nkv + it.g) * kHD;
+    float lo[8], hi[8], c[8], sv[8];
+    load8f(base + 8 * l8, lo);
+    load8f(base + 64 + 8 * l8, hi);
+    const bool rope = is_k && p.has_rotary;
+    if (rope) {
+      const long long cb = (long long)j * (kHD / 2) + 8 * l8;
+      load8f(reinterpret_cast<const float*>(p.cos_c) + cb, c);
+      load8f(reinterpret_cast<const float*>(p.sin_c) + cb, sv);
+    }
+    // Every lane takes part in the norm's shuffles; V rows keep their values.
+    float klo[8], khi[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      klo[k] = lo[k];
+      khi[k] = hi[k];
+    }
+    norm_rope8(p, klo, khi, wlo, whi, p.has_norm, false, c, sv);
+    if (is_k && p.has_norm) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        lo[k] = klo[k];
+        hi[k] = khi[k];
+      }
+    }
+    if (rope) norm_rope8(p, lo, hi, wlo, whi, false, true, c, sv);
+    if (mine) {
+      const float* scp = is_k ? p.k_scale : p.v_scale;
+      const int nsc = is_k ? p.k_scale_n : p.v_scale_n;
+      float slo[8], shi[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        slo[k] = channel_scale(scp, nsc, it.g * kHD + 8 * l8 + k);
+        shi[k] = channel_scale(scp, nsc, it.g * kHD + 64 + 8 * l8 + k);
+      }
+      int8_t* dst = reinterpret_cast<int8_t*>(is_k ? p.present_k : p.present_v) +
+                    (((long long)it.b * p.Nkv + it.g) * p.C + j) * kHD;
+      *reinterpret_cast<uint2*>(dst + 8 * l8) = quant8(lo, slo);
+      *reinterpret_cast<uint2*>(dst + 64 + 8 * l8) = quant8(hi, shi);
+    }
+  }
+}
+
+// One int8 tile (128 rows x 128 codes, 128-byte swizzle as TMA wrote it) as
+// the fp16 operand tile (two 64-column boxes, 128-byte swizzle). Converter
+// thread t takes row t. int8 -> fp16 without the conversion unit: the byte
+// c+128 as the low mantissa bits of 1024.0 (fp16 0x6400) is 1152 + c exactly.
+__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int t) {
+  const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {   // 16-byte chunk c: codes 16c .. 16c+15
+    const uint4 w = *reinterpret_cast<const uint4*>(src + sw128_offset(t, c));
+    const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t p01 = __byte_perm(wv[k], 0x64646464u, 0x4140u);
+      const uint32_t p23 = __byte_perm(wv[k], 0x64646464u, 0x4342u);
+      const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&p01), bias);
+      const __half2 b2 = __hsub2(*reinterpret_cast<const __half2*>(&p23), bias);
+      h[2 * k] = *reinterpret_cast<const uint32_t*>(&a);
+      h[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    const int col = 16 * c, bx = col >> 6, ch = (col & 63) >> 3;
+    *reinterpret_cast<uint4*>(dst + bx * kBox + sw128_offset(t, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(dst + bx * kBox + sw128_offset(t, ch + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+// Output value of row r, dim d from (m, l, o): sink / smooth-softmax term, 1/l, fp16.
+__device__ __forceinline__ void write_out(const Params& p, int b, int g, int total, int r, int d, float m, float l,
+                                          float o) {
+  const int i = r / p.G, h = g * p.G + r % p.G;
+  const long long oi = ((long long)(b * p.S + i) * p.N + h) * kHD + d;
+  float val;
+  if (p.mode == kPrompt && i >= total) {
+    val = 0.f;
+  } else {
+    float mf = m, extra = 0.f;
+    if (p.has_sink || p.smooth) {
+      const float sg = (p.has_sink ? load_t(p.sink, h, p.t_type) : 0.f) * kLog2e;
+      mf = fmaxf(m, sg);
+      extra = ex2(sg - mf);
+    }
+    const float f = ex2(m - mf);
+    const float den = l * f + extra;
+    val = den > 0.f ? o * f / den : 0.f;
+  }
+  reinterpret_cast<float*>(p.out)[oi] = val;
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int R, bool kPlain>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ uint8_t smem_raw[];
+  DSmem& sm = *reinterpret_cast<DSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // The preparer's first global loads overlap the set-up below.
+  long long ntot = 0;
+  if (warp == 2) ntot = count_units(p, blockIdx.x == 0);
+  if (warp == 1) tmem_alloc(&sm.tmem, 64);
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&sm.kfull[s], 1);
+      mbar_init(&sm.kempty[s], kConv);   // every converter thread read its row
+    }
+    for (int s = 0; s < kNSV; ++s) {
+      mbar_init(&sm.vfull[s], 1);
+      mbar_init(&sm.vempty[s], kConv);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.k16full[s], kConv);
+      mbar_init(&sm.k16empty[s], 1);     // MMA commit after S
+      mbar_init(&sm.v16full[s], kConv);
+      mbar_init(&sm.v16empty[s], 1);     // MMA commit after P.V
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.imap[s], 1);
+      mbar_init(&sm.iready[s], 1);
+      mbar_init(&sm.iempty[s], 2);  // MMA commit (Q^T reads done) + softmax release
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.s_free[s], kSoft);
+      mbar_init(&sm.p_full[s], kSoft);
+      mbar_init(&sm.p_free[s], 1);
+    }
+    mbar_init(&sm.o_full, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    sm.last = 0;
+    mbar_fence_init();
+  }
+  // Query / probability rows >= R are zero for the whole kernel.
+  for (int x = tid; x < (int)(2 * 2 * kRowBox / 16); x += kThreads) {
+    reinterpret_cast<uint4*>(&sm.qt[0][0])[x] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(&sm.pt[0][0])[x] = make_uint4(0, 0, 0, 0);
+  }
+  fence_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+
+  if (warp == 2) {
+    // ================================================================ preparer
+    // With fewer tiles than CTAs only the first `ntot` CTAs work, so that
+    // every working CTA's share is non-empty and the CTAs sharing a (b, g)
+    // are consecutive.
+    const long long nc = ntot < (long long)gridDim.x ? ntot : (long long)gridDim.x;
+    long long t = 0, tend = 0;
+    if ((long long)blockIdx.x < nc) {
+      t = share_start(blockIdx.x, ntot, nc);
+      tend = share_start(blockIdx.x + 1, ntot, nc);
+    }
+    int slot = 0;
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    while (true) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iempty[slot], iphase[slot] ^ 1u)) || aborted(sm)) {
+        ok = false;
+        break;
+      }
+      DItem it;
+      it.end = 1;
+      while (t < tend) {
+        map_segment(p, t, tend, ntot, nc, it);
+        if (it.end != 2) break;
+        t += it.ntiles;
+        it.end = 1;
+      }
+      if (t >= tend) {
+        if (lane == 0) {
+          sm.item[slot].end = 1;
+          mbar_arrive(&sm.imap[slot]);
+          mbar_arrive(&sm.iready[slot]);
+        }
+        break;
+      }
+      if (it.end) {   // unreachable: every t < ntot maps to a unit
+        ok = false;
+        break;
+      }
+      t += it.ntiles;
+      // The TMA warp may stream the segment's cached tiles while the query
+      // rows are prepared; tiles holding new rows wait for `iready`.
+      if (lane == 0) {
+        sm.item[slot] = it;
+        mbar_arrive(&sm.imap[slot]);
+      }
+      prepare_qt(p, it, R, sm.qt[slot], sm.qpow[slot]);
+      append_rows(p, it);
+      fence_async_all();  // query rows (shared) and appended rows (global) -> async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.iready[slot]);
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+  } else if (warp == 0) {
+    // ================================================================ TMA
+    // K and V tiles have their own stages: K(u) is released as soon as
+    // S(u) is done, V(u) after O += V P(u).
+    int slot = 0, tau = 0, nk = 0, nv = 0;   // tiles begun; K and V fills issued
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    while (ok) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.imap[slot], iphase[slot]))) {
+        ok = false;
+        break;
+      }
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      const int row0 = (it.b * p.Nkv + it.g) * p.C + it.j0;
+      bool ready = false;
+      for (int t = 0; t < it.ntiles; ++t, ++tau) {
+        const int st = tau % kNS, sv = tau % kNSV;
+        const uint32_t par = ((uint32_t)(tau / kNS) & 1u) ^ 1u, parv = ((uint32_t)(tau / kNSV) & 1u) ^ 1u;
+        if (!ready && it.j0 + (t + 1) * kKT > it.past) {   // the tile holds new rows
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot]))) {
+            ok = false;
+            break;
+          }
+          ready = true;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kempty[st], par)) || aborted(sm)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_tx(&sm.kfull[st], kTile8);
+          tma_load_2d(sm.k8[st], &tmk, 0, row0 + t * kKT, &sm.kfull[st]);
+        }
+        __syncwarp();
+        ++nk;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vempty[sv], parv)) || aborted(sm)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_tx(&sm.vfull[sv], kTile8);
+          tma_load_2d(sm.v8[sv], &tmv, 0, row0 + t * kKT, &sm.vfull[sv]);
+        }
+        __syncwarp();
+        ++nv;
+      }
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+    // Drain: every fill this warp issued has landed before the CTA can exit
+    // (older fills completed before their stage was refilled).
+    for (int u = max(0, nk - kNS); u < nk; ++u) mbar_wait(&sm.kfull[u % kNS], (uint32_t)(u / kNS) & 1u);
+    for (int u = max(0, nv - kNSV); u < nv; ++u) mbar_wait(&sm.vfull[u % kNSV], (uint32_t)(u / kNSV) & 1u);
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    int slot = 0, tau = 0;
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    auto issue_pv = [&](int u, bool acc) {
+      const int pb = u & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
+                                       mbar_wait(&sm.v16full[pb], (uint32_t)(u >> 1) & 1u)))
+        return false;
+      if (lane == 0) {
+        tc_fence_after();
+        for (int ks = 0; ks < 8; ++ks)
+          mma_f16_ss(tmem + 32, desc_mnmajor_sw128(smem_addr(sm.v[pb]) + ks * 2048, kBox, 1024),
+                     desc_kmajor_sw128(smem_addr(sm.pt[pb] + (ks >> 2) * kRowBox) + (ks & 3) * 32), kIdO,
+                     acc || ks > 0);
+        mma_commit(&sm.p_free[pb]);
+        mma_commit(&sm.v16empty[pb]);
+      }
+      __syncwarp();
+      return true;
+    };
+    while (ok) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot]))) {
+        ok = false;
+        break;
+      }
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      for (int t = 0; t < it.ntiles && ok; ++t) {
+        const int u = tau + t, kb = u & 1, sb = u & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.k16full[kb], (uint32_t)(u >> 1) & 1u) &&
+                                         mbar_wait(&sm.s_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t koff = (ks & 3) * 32;
+            mma_f16_ss(tmem + sb * 16, desc_kmajor_sw128(smem_addr(sm.k[kb] + (ks >> 2) * kBox) + koff),
+                       desc_kmajor_sw128(smem_addr(sm.qt[slot] + (ks >> 2) * kRowBox) + koff), kIdS, ks > 0);
+          }
+          mma_commit(&sm.s_full[sb]);
+          mma_commit(&sm.k16empty[kb]);
+        }
+        __syncwarp();
+        if (t > 0 && !issue_pv(u - 1, t - 1 > 0)) ok = false;
+      }
+      if (ok && it.ntiles > 0 && !issue_pv(tau + it.ntiles - 1, it.ntiles > 1)) ok = false;
+      if (!ok) break;
+      if (lane == 0) {
+        mma_commit(&sm.o_full);
+        mma_commit(&sm.iempty[slot]);
+      }
+      __syncwarp();
+      tau += it.ntiles;
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+      if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+    if (lane == 0) {
+      mma_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= kConvWarp0) {
+    // ================================================================ converters
+    const int ct = tid - kConvWarp0 * 32;   // row of the tile this thread converts
+    int slot = 0, u = 0;
+    uint32_t iphase[2] = {0, 0};
+    bool ok = true;
+    while (ok) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.imap[slot], iphase[slot]))) {
+        ok = false;
+        break;
+      }
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      for (int t = 0; t < it.ntiles; ++t, ++u) {
+        const int st = u % kNS, kb = u & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[st], (uint32_t)(u / kNS) & 1u) &&
+                                         mbar_wait(&sm.k16empty[kb], ((uint32_t)(u >> 1) & 1u) ^ 1u)) ||
+            aborted(sm)) {
+          ok = false;
+          break;
+        }
+        convert_tile(sm.k8[st], sm.k[kb], ct);
+        fence_async_smem();
+        mbar_arrive(&sm.k16full[kb]);
+        mbar_arrive(&sm.kempty[st]);
+        const int sv = u % kNSV;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vfull[sv], (uint32_t)(u / kNSV) & 1u) &&
+                                         mbar_wait(&sm.v16empty[kb], ((uint32_t)(u >> 1) & 1u) ^ 1u)) ||
+            aborted(sm)) {
+          ok = false;
+          break;
+        }
+        convert_tile(sm.v8[sv], sm.v[kb], ct);
+        fence_async_smem();
+        mbar_arrive(&sm.v16full[kb]);
+        mbar_arrive(&sm.vempty[sv]);
+      }
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+    }
+    if (!ok && lane == 0) set_abort(p, sm);
+  } else {
+    // ================================================================ softmax
+    // A warp never leaves the loop except right after a named barrier at
+    // which every softmax warp reads the same abort flag.
+    const int quarter = warp & 3;
+    const int kl = quarter * 32 + lane;           // tensor-memory lane: key of the tile, dim of O^T
+    const int ws = warp - kSoftWarp0;             // softmax warp index 0..3
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int rows = p.S * p.G;
+    int slot = 0, tau = 0, icount = 0;
+    uint32_t iphase[2] = {0, 0};
+    while (true) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
+      named_sync();
+      if (aborted(sm)) break;
+      const DItem it = sm.item[slot];
+      if (it.end) break;
+      const int b = it.b, g = it.g;
+      int pos_r[R], ih_r[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int i = r < rows ? r / p.G : 0;
+        pos_r[r] = it.past + i;
+        ih_r[r] = r < rows ? i * p.N + g * p.G + r % p.G : -1;
+      }
+      float m_run[R], l_part[R], qp[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        m_run[r] = kNegBig;
+        l_part[r] = 0.f;
+        qp[r] = r < rows ? sm.qpow[slot][r] : 1.f;
+      }
+      // V channel scale of this thread's output dim (applied once to O).
+      const float vsc = channel_scale(p.v_scale, p.v_scale_n, g * kHD + kl);
+      bool bad = false;
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int u = tau + t, sb = u & 1;
+        const int jk = it.j0 + t * kKT + kl;      // this thread's key
+        const bool key_ok = jk < it.jend;
+        float s[R];
+        bool got = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (uint32_t)(u >> 1) & 1u));
+        if (got) {
+          tc_fence_after();
+          uint32_t raw[16];
+          tmem_ld16(tmem + lane_addr + sb * 16, raw);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&sm.s_free[sb]);
+          // (V rows past the key range hold int8 codes, finite, and get P = 0.)
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float x = (__uint_as_float(raw[r]) + __uint_as_float(raw[r + R])) * qp[r];   // hi + lo rows
+            bool vis = key_ok && ih_r[r] >= 0;
+            if (p.causal) vis = vis && jk <= pos_r[r];
+            if (p.window >= 0) vis = vis && jk >= pos_r[r] - p.window;
+            if (!kPlain && p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap) * kLog2e;
+            if (!kPlain && p.has_bias && vis) {
+              const int i = ih_r[r] / p.N, h = ih_r[r] % p.N;
+              const long long bi =
+                  (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
+                      p.bias_ld + jk;
+              x += load_t(p.bias, bi, p.t_type) * kLog2e;
+            }
+            s[r] = vis ? x : kNegBig;
+            float m = s[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) sm.red[sb][ws][r] = m;
+          }
+        } else if (lane == 0) {
+          set_abort(p, sm);
+        }
+        named_sync();
+        if (aborted(sm)) {
+          bad = true;
+          break;
+        }
+        // Tile max per row; lazy rescale of O^T (only after the item's first tile).
+        float mt[R];
+        bool any_grow = false;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          mt[r] = fmaxf(fmaxf(sm.red[sb][0][r], sm.red[sb][1][r]), fmaxf(sm.red[sb][2][r], sm.red[sb][3][r]));
+          any_grow = any_grow || mt[r] > m_run[r] + kLazy;
+        }
+        if (any_grow && t > 0) {
+          // O^T must hold P.V up to tile t-1.
+          const int pu = u - 1;
+          if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[pu & 1], (uint32_t)(pu >> 1) & 1u))) {
+            tc_fence_after();
+            uint32_t o[16];
+            tmem_ld16(tmem + lane_addr + 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              if (mt[r] > m_run[r] + kLazy) {
+                const float f = ex2(m_run[r] - mt[r]);
+                o[r] = __float_as_uint(__uint_as_float(o[r]) * f);
+                o[r + R] = __float_as_uint(__uint_as_float(o[r + R]) * f);
+                l_part[r] *= f;
+              }
+            }
+            tmem_st16(tmem + lane_addr + 32, o);
+            tmem_st_wait();
+          } else if (lane == 0) {
+            set_abort(p, sm);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (mt[r] > m_run[r] + kLazy) m_run[r] = mt[r];
+        // P^T(u): its buffer is free once P.V(u-2) finished.
+        if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float pr = s[r] <= kNegBig ? 0.f : ex2(s[r] - m_run[r]);
+            l_part[r] += pr;
+            const __half ph = __float2half_rn(pr);
+            *reinterpret_cast<__half*>(sm.pt[sb] + sw_elem(r, kl, kRowBox)) = ph;
+            *reinterpret_cast<__half*>(sm.pt[sb] + sw_elem(r + R, kl, kRowBox)) =
+                __float2half_rn(pr - __half2float(ph));
+          }
+        } else if (lane == 0) {
+          set_abort(p, sm);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[sb]);
+      }
+      if (bad) break;
+      tau += it.ntiles;
+      // ---- end of item: O^T row kl = dim kl of every query row
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.o_full, (uint32_t)icount & 1u));
+      uint32_t o[16];
+      if (got) {
+        tc_fence_after();
+        tmem_ld16(tmem + lane_addr + 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          o[r] = __float_as_uint((__uint_as_float(o[r]) + __uint_as_float(o[r + R])) * vsc);
+      } else if (lane == 0) {
+        set_abort(p, sm);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float l = l_part[r];
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
+        if (lane == 0) sm.redl[ws][r] = l;
+      }
+      named_sync();
+      if (aborted(sm)) break;
+      const int bg = b * p.Nkv + g;
+      if (it.nsplit == 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r >= rows) continue;
+          const float l = sm.redl[0][r] + sm.redl[1][r] + sm.redl[2][r] + sm.redl[3][r];
+          write_out(p, b, g, it.total, r, kl, m_run[r], l, __uint_as_float(o[r]));
+        }
+      } else {
+        const long long pbase = (long long)it.slot * p.rows_pad;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if (r >= rows) continue;
+          p.part_o[(pbase + r) * kHD + kl] = __uint_as_float(o[r]);
+          if (kl == 0) {
+            p.part_ml[(pbase + r) * 2] = m_run[r];
+            p.part_ml[(pbase + r) * 2 + 1] = sm.redl[0][r] + sm.redl[1][r] + sm.redl[2][r] + sm.redl[3][r];
+          }
+        }
+        named_sync();
+        if (tid == kSoftWarp0 * 32) {   // first softmax thread
+          const unsigned ticket = ticket_acq_rel(&p.counters[bg]);
+          sm.last = ticket == (unsigned)(it.nsplit - 1);
+        }
+        named_sync();
+        if (sm.last) {
+          // One pass over the splits (online merge); the loads of a split for
+          // all rows are independent, so they are in flight together.
+          float M[R], Ls[R], A[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            M[r] = kNegBig;
+            Ls[r] = 0.f;
+            A[r] = 0.f;
+          }
+          for (int s2 = 0; s2 < it.nsplit; ++s2) {
+            const long long sb0 = (long long)(s2 == 0 ? it.slot0 : 2 * (it.cfirst + s2)) * p.rows_pad;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              if (r >= rows) continue;
+              const float m = __ldcg(&p.part_ml[(sb0 + r) * 2]);
+              const float l = __ldcg(&p.part_ml[(sb0 + r) * 2 + 1]);
+              const float ov = __ldcg(&p.part_o[(sb0 + r) * kHD + kl]);
+              const float mn = fmaxf(M[r], m);
+              const float fa = ex2(M[r] - mn), fb = ex2(m - mn);
+              Ls[r] = Ls[r] * fa + l * fb;
+              A[r] = A[r] * fa + ov * fb;
+              M[r] = mn;
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            if (r < rows) write_out(p, b, g, it.total, r, kl, M[r], Ls[r], A[r]);
+          if (tid == kSoftWarp0 * 32) p.counters[bg] = 0;  // ready for the next call
+        }
+        named_sync();
+        if (tid == kSoftWarp0 * 32) sm.last = 0;
+      }
+      named_sync();   // slot, reduction buffers and the ticket flag are free again
+      if (tid == kSoftWarp0 * 32) mbar_arrive(&sm.iempty[slot]);
+      iphase[slot] ^= 1u;
+      slot ^= 1;
+      ++icount;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 64);
+}
+
+// Per-device launch facts, looked up on the first launch on each device
+// (racing first calls store the same values).
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+bool g_smem_set[10][kMaxDevices];
+
+static_assert(sizeof(DSmem) + 1024 <= 232448, "shared memory of one CTA");
+
+template <int R, bool kPlain>
+cudaError_t launch_rp(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv, int ri) {
+  const int smem = (int)sizeof(DSmem) + 1024;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_smem_set[ri][dev]) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<R, kPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    g_smem_set[ri][dev] = true;
+  }
+  if (g_sm_count[dev] == 0) {
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    g_sm_count[dev] = sms;
+  }
+  const int sms = g_sm_count[dev];
+  const int grid = sms < kTcDecodeMaxCtas ? sms : kTcDecodeMaxCtas;
+  decode_tc_kernel<R, kPlain><<<grid, kThreads, smem, st>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+// Scores without softcap or bias take a kernel whose tile loop has no code
+// for them.
+template <int R>
+cudaError_t launch_r(const Params& p, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv, int ri) {
+  if (p.softcap > 0.f || p.has_bias) return launch_rp<R, false>(p, st, mk, mv, ri);
+  return launch_rp<R, true>(p, st, mk, mv, ri + 5);
+}
+
+}  // namespace
+
+bool decode_tc_i8_supported(const Params& p) {
+  return p.t_type == kF32 && p.cache_type == kI8 && p.H == kHD && 2 * p.S * p.G <= kNR;
+}
+
+cudaError_t prepare_decode_tc_i8(const Params& p, TmaMaps* maps) {
+  const long long krows = (long long)p.B * p.Nkv * p.C;
+  cudaError_t e = encode_u8_2d_sw128(&maps->m[0], p.present_k, (uint64_t)krows, kHD, kHD, kHD, kKT);
+  if (e != cudaSuccess) return e;
+  return encode_u8_2d_sw128(&maps->m[1], p.present_v, (uint64_t)krows, kHD, kHD, kHD, kKT);
+}
+
+cudaError_t launch_decode_tc_i8(const Params& p, cudaStream_t st, const TmaMaps& maps) {
+  const CUtensorMap& mk = maps.m[0];
+  const CUtensorMap& mv = maps.m[1];
+  switch (p.rows_pad) {
+    case 1: return launch_r<1>(p, st, mk, mv, 0);
+    case 2: return launch_r<2>(p, st, mk, mv, 1);
+    case 4: return launch_r<4>(p, st, mk, mv, 2);
+    case 8: return launch_r<8>(p, st, mk, mv, 3);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gqa

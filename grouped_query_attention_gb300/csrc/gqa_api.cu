@@ -72,7 +72,8 @@ struct Plan {
   gqa::Params P;
   bool decode;
   bool tensor_core;  // prefill on the tcgen05 kernel (fp16, head size 128)
-  bool tc_decode;    // decode on the tcgen05 kernel (fp16 cache, head size 128, <= 16 rows)
+  bool tc_decode;    // decode on a tcgen05 kernel (fp16 cache <= 16 rows, or int8 cache with fp32 <= 8 rows; H=128)
+  bool tc_i8;        // ... the int8-cache one
   size_t hdr_bytes, qprep_bytes, part_bytes, total_bytes;
   size_t part_rows;  // decode partial rows (part_o holds part_rows x H floats, part_ml part_rows x 2)
 };
@@ -272,7 +273,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
 
   // ---- regime and workspace plan
   pl->decode = gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P));
-  pl->tc_decode = pl->decode && gqa::decode_tc_supported(P);
+  pl->tc_i8 = pl->decode && gqa::decode_tc_i8_supported(P);
+  pl->tc_decode = pl->decode && (gqa::decode_tc_supported(P) || pl->tc_i8);
   pl->tensor_core = false;
   pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));  // status, tickets
   pl->qprep_bytes = 0;
@@ -342,6 +344,12 @@ cudaError_t timed_launch(gqa_handle* h, int kind, cudaStream_t st, F fn) {
     h->kinds[h->used++] = kind;
   }
   return e;
+}
+
+// The decode launch a plan selected.
+cudaError_t launch_decode_any(const Plan& pl, cudaStream_t st, const gqa::TmaMaps& maps) {
+  if (!pl.tc_decode) return gqa::launch_decode(pl.P, st);
+  return pl.tc_i8 ? gqa::launch_decode_tc_i8(pl.P, st, maps) : gqa::launch_decode_tc(pl.P, st, maps);
 }
 
 }  // namespace
@@ -437,7 +445,7 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   cudaError_t e = cudaSuccess;
   gqa::TmaMaps maps;   // host work of the tensor-core launches, done before the first launch
   if (pl.decode && pl.tc_decode)
-    e = gqa::prepare_decode_tc(P, &maps);
+    e = pl.tc_i8 ? gqa::prepare_decode_tc_i8(P, &maps) : gqa::prepare_decode_tc(P, &maps);
   else if (!pl.decode && pl.tensor_core)
     e = gqa::prepare_prefill_tc(P, &maps);
   if (e != cudaSuccess) return cuda_fail(e, "TMA tensor maps");
@@ -447,7 +455,7 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   }
   if (pl.decode) {
     e = timed_launch(h, pl.tc_decode ? GQA_KERNEL_DECODE_TENSOR_CORE : GQA_KERNEL_DECODE, st,
-                     [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st, maps) : gqa::launch_decode(P, st); });
+                     [&] { return launch_decode_any(pl, st, maps); });
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   } else {
     e = timed_launch(h, GQA_KERNEL_PREPASS, st, [&] { return gqa::launch_prepass(P, st); });
@@ -480,13 +488,15 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
   if (e != cudaSuccess) return cuda_fail(e, "scratch header clear");
   const gqa::Params& P = pl.P;
   gqa::TmaMaps maps;
-  if (pl.tc_decode && (e = gqa::prepare_decode_tc(P, &maps)) != cudaSuccess) return cuda_fail(e, "TMA tensor maps");
+  if (pl.tc_decode &&
+      (e = pl.tc_i8 ? gqa::prepare_decode_tc_i8(P, &maps) : gqa::prepare_decode_tc(P, &maps)) != cudaSuccess)
+    return cuda_fail(e, "TMA tensor maps");
   if (P.mode == gqa::kCopy) {
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }
   e = timed_launch(h, pl.tc_decode ? GQA_KERNEL_DECODE_TENSOR_CORE : GQA_KERNEL_DECODE, st,
-                   [&] { return pl.tc_decode ? gqa::launch_decode_tc(P, st, maps) : gqa::launch_decode(P, st); });
+                   [&] { return launch_decode_any(pl, st, maps); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return GQA_OK;
 }

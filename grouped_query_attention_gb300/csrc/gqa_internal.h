@@ -93,6 +93,10 @@ struct TmaMaps {
 };
 cudaError_t prepare_decode_tc(const Params& p, TmaMaps* maps);
 cudaError_t launch_decode_tc(const Params& p, cudaStream_t st, const TmaMaps& maps);
+// Tensor-core decode for an int8 cache with fp32 queries (head size 128, <= 8 rows).
+bool decode_tc_i8_supported(const Params& p);
+cudaError_t prepare_decode_tc_i8(const Params& p, TmaMaps* maps);
+cudaError_t launch_decode_tc_i8(const Params& p, cudaStream_t st, const TmaMaps& maps);
 // The tensor-core decode runs min(SM count, kTcDecodeMaxCtas) persistent CTAs
 // and keeps two partial slots per CTA.
 constexpr int kTcDecodeMaxCtas = 256;

@@ -14,4 +14,9 @@ namespace gqa {
 cudaError_t encode_fp16_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                                  uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
 
+// The same for a row-major [rows][cols] matrix of bytes (int8 codes): boxes of
+// box_cols (<= 128) x box_rows bytes with the 128-byte swizzle.
+cudaError_t encode_u8_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                               uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+
 }  // namespace gqa

@@ -53,6 +53,15 @@ DECODE = {
     # new rows straddling a 128-key tile boundary (keys 1022..1025), S*G = 16
     "f16_tc_s4_straddle": spec(S=4, N=16, Nkv=4, capacity=1100, seqlens_k=(1025, 130, 3), seqlens_range=None,
                                rotary_theta=1e4, qk_norm=True),
+    # tensor-core decode for int8 caches with fp32 queries (head size 128, up to 8 rows per KV head)
+    "i8_tc_per_tensor_s2_copy_norm_rotary": spec(dtype="f32", N=8, Nkv=2, S=2, mode="copy", past_len=600,
+                                                  seqlens_range=(50, 590), quant="PER_TENSOR", qk_norm=True,
+                                                  rotary_theta=1e4, scale_range=(0.02, 0.04)),
+    "i8_tc_all_features": spec(dtype="f32", N=8, Nkv=4, quant="PER_CHANNEL", seqlens_range=(1, 700),
+                               local_window_size=200, softcap=30.0, bias=(3, 8, 0.5), head_sink=True, qk_norm=True,
+                               rotary_theta=1e4),
+    "i8_tc_one_head_long": spec(dtype="f32", B=1, N=8, Nkv=1, capacity=20000, seqlens_range=(19000, 19990),
+                                quant="PER_CHANNEL"),
 }
 
 PREFILL = {
