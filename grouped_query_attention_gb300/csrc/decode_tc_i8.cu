@@ -5,7 +5,9 @@
 // tiles over persistent CTAs, S^T = K Q^T and O^T += V^T P^T per tile in
 // tensor memory, one softmax thread per key), with two additions:
 //   - int8 codes are exact in fp16, so TMA brings the int8 K / V tiles and
-//     four converter warps (7..10) rewrite them as fp16 MMA operand tiles;
+//     four converter warps (7..10) rewrite them in fp16: K straight into
+//     tensor memory (the A operand of S^T, one key per lane), V into one of
+//     two shared-memory operand tiles;
 //   - fp32 accuracy: each prepared query row q' (norm, rotary, scale, K
 //     channel scale folded in, times a power of two 2^-e that brings its
 //     largest value to [1, 2)) is split into two fp16 rows hi = fp16(q'),
@@ -13,9 +15,9 @@
 //     codes are exact and accumulate in fp32, so S = (S_hi + S_lo) 2^e holds
 //     q' to about 2^-22. Probabilities are split the same way for P.V, and
 //     the V channel scale multiplies O once at the end.
-// Warp roles: 0 TMA (int8 tiles, 3 stages each for K and V), 1 MMA, 2
+// Warp roles: 0 TMA (int8 tiles, 4 stages each for K and V), 1 MMA, 2
 // preparer (segments, query rows, appended int8 rows), 3..6 softmax, 7..10
-// converters (K into one of two fp16 buffers, V into one).
+// converters (thread = tensor-memory lane = key row of the tile).
 //
 // com.microsoft.GroupQueryAttention, section Implementation variants
 // (quant_int8_decode_splitk: int8 rows appended with k/v_scale, attention over
@@ -35,8 +37,8 @@ using namespace tc;
 constexpr int kHD = 128;
 constexpr int kKT = kTcDecodeTile;       // keys per tile (128)
 constexpr int kNR = 16;                  // MMA N: hi and lo query rows of the group, padded
-constexpr int kNS = 3;                   // int8 K stages
-constexpr int kNSV = 2;                  // int8 V stages
+constexpr int kNS = 4;                   // int8 K stages
+constexpr int kNSV = 4;                  // int8 V stages
 constexpr int kThreads = 352;            // TMA, MMA, preparer, 4 softmax, 4 converter warps
 constexpr int kSoftWarp0 = 3;            // first softmax warp
 constexpr int kConvWarp0 = 7;            // first converter warp
@@ -49,7 +51,11 @@ constexpr uint32_t kRowBox = 16u * 128u; // 64 columns x 16 rows = 2 KB
 constexpr float kLazy = 8.0f;            // log2 growth tolerated before rescaling O
 constexpr uint32_t kIdS = idesc_f16(128, kNR, 0, 0);   // K (K-major) x Q^T rows (K-major)
 constexpr uint32_t kIdO = idesc_f16(128, kNR, 1, 0);   // V (MN-major) x P^T rows (K-major)
-// Tensor memory: S^T buffers at columns 0 and 16, O^T at 32 (16 columns each).
+// Tensor memory (256 columns): S^T buffers at columns 0 and 16, O^T at 32
+// (16 columns each), fp16 K tiles (A operand of S^T, one key per lane, two
+// dims per column) at columns 64 and 128.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kKCol = 64;
 
 struct DItem {
   int b, g;
@@ -64,7 +70,6 @@ struct DItem {
 struct __align__(1024) DSmem {
   uint8_t k8[kNS][kTile8];      // int8 tiles as loaded (128-byte swizzle)
   uint8_t v8[kNSV][kTile8];
-  uint8_t k[2][kTile];          // fp16 K operand tiles (two buffers)
   uint8_t v[2][kTile];          // fp16 V operand tiles (two buffers)
   uint8_t qt[2][2 * kRowBox];   // per item slot: hi / lo query rows (16 x 128, fp16, swizzled)
   uint8_t pt[2][2 * kRowBox];   // P^T buffers: hi / lo rows x 128 keys (fp16, swizzled)
@@ -440,6 +445,32 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
   }
 }
 
+// One K row of an int8 tile as fp16 pairs in 64 tensor-memory columns of this
+// thread's lane (lane = key row; warp w owns lanes 32 (w % 4) ..).
+__device__ __forceinline__ void convert_k_row_to_tmem(const uint8_t* src, int t, uint32_t taddr) {
+  const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+#pragma unroll
+  for (int hlf = 0; hlf < 2; ++hlf) {
+    uint32_t h[32];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {   // chunk c = 4 hlf + c4: codes 16c .. 16c+15
+      const int c = 4 * hlf + c4;
+      const uint4 w = *reinterpret_cast<const uint4*>(src + sw128_offset(t, c));
+      const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t p01 = __byte_perm(wv[k], 0x64646464u, 0x4140u);
+        const uint32_t p23 = __byte_perm(wv[k], 0x64646464u, 0x4342u);
+        const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&p01), bias);
+        const __half2 b2 = __hsub2(*reinterpret_cast<const __half2*>(&p23), bias);
+        h[8 * c4 + 2 * k] = *reinterpret_cast<const uint32_t*>(&a);
+        h[8 * c4 + 2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+    }
+    tmem_st32(taddr + 32 * hlf, h);
+  }
+}
+
 // Output value of row r, dim d from (m, l, o): sink / smooth-softmax term, 1/l, fp16.
 __device__ __forceinline__ void write_out(const Params& p, int b, int g, int total, int r, int d, float m, float l,
                                           float o) {
@@ -474,7 +505,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
   // The preparer's first global loads overlap the set-up below.
   long long ntot = 0;
   if (warp == 2) ntot = count_units(p, blockIdx.x == 0);
-  if (warp == 1) tmem_alloc(&sm.tmem, 64);
+  if (warp == 1) tmem_alloc(&sm.tmem, kTmemCols);
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&sm.kfull[s], 1);
@@ -666,7 +697,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           tc_fence_after();
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t koff = (ks & 3) * 32;
-            mma_f16_ss(tmem + sb * 16, desc_kmajor_sw128(smem_addr(sm.k[kb] + (ks >> 2) * kBox) + koff),
+            mma_f16_ts(tmem + sb * 16, tmem + kKCol + kb * 64 + ks * 8,
                        desc_kmajor_sw128(smem_addr(sm.qt[slot] + (ks >> 2) * kRowBox) + koff), kIdS, ks > 0);
           }
           mma_commit(&sm.s_full[sb]);
@@ -695,7 +726,9 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     __syncwarp();
   } else if (warp >= kConvWarp0) {
     // ================================================================ converters
-    const int ct = tid - kConvWarp0 * 32;   // row of the tile this thread converts
+    // Row of the tile this thread converts = its tensor-memory lane.
+    const int ct = (warp & 3) * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
     int slot = 0, u = 0;
     uint32_t iphase[2] = {0, 0};
     bool ok = true;
@@ -714,8 +747,9 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        convert_tile(sm.k8[st], sm.k[kb], ct);
-        fence_async_smem();
+        convert_k_row_to_tmem(sm.k8[st], ct, tmem + lane_addr + kKCol + kb * 64);
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&sm.k16full[kb]);
         mbar_arrive(&sm.kempty[st]);
         const int sv = u % kNSV;
@@ -954,7 +988,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 64);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
 // Per-device launch facts, looked up on the first launch on each device
