@@ -573,6 +573,19 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     int slot = 0, tau = 0;
     uint32_t iphase[2] = {0, 0};
     bool ok = true;
+    // Shared-memory descriptors of every operand buffer, built once; a K step
+    // adds its start-address offset (16-byte units) to the descriptor.
+    uint64_t dq[2], dp[2], dk[kNS], dv[kNS];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      dq[i] = desc_kmajor_sw128(smem_addr(sm.qt[i]));
+      dp[i] = desc_kmajor_sw128(smem_addr(sm.pt[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < kNS; ++i) {
+      dk[i] = desc_kmajor_sw128(smem_addr(sm.k[i]));
+      dv[i] = desc_mnmajor_sw128(smem_addr(sm.v[i]), kBox, 1024);
+    }
     auto issue_pv = [&](int u, bool acc) {
       const int st = u % kNS, pb = u & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
@@ -580,9 +593,10 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         return false;
       if (lane == 0) {
         tc_fence_after();
+        const uint64_t a0 = dv[st], b0 = dp[pb];
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_f16_ss(tmem + 32, desc_mnmajor_sw128(smem_addr(sm.v[st]) + ks * 2048, kBox, 1024),
-                     desc_kmajor_sw128(smem_addr(sm.pt[pb] + (ks >> 2) * kRowBox) + (ks & 3) * 32), kIdO,
+          mma_f16_ss(tmem + 32, a0 + (uint64_t)(ks * 128), b0 + (uint64_t)((ks >> 2) * 128 + (ks & 3) * 2), kIdO,
                      acc || ks > 0);
         mma_commit(&sm.p_free[pb]);
         mma_commit(&sm.vempty[st]);
@@ -606,11 +620,11 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         }
         if (lane == 0) {
           tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t koff = (ks & 3) * 32;
-            mma_f16_ss(tmem + sb * 16, desc_kmajor_sw128(smem_addr(sm.k[st] + (ks >> 2) * kBox) + koff),
-                       desc_kmajor_sw128(smem_addr(sm.qt[slot] + (ks >> 2) * kRowBox) + koff), kIdS, ks > 0);
-          }
+          const uint64_t a0 = dk[st], b0 = dq[slot];
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ss(tmem + sb * 16, a0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                       b0 + (uint64_t)((ks >> 2) * 128 + (ks & 3) * 2), kIdS, ks > 0);
           mma_commit(&sm.s_full[sb]);
           mma_commit(&sm.kempty[st]);
         }

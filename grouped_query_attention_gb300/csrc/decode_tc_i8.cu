@@ -662,6 +662,15 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     int slot = 0, tau = 0;
     uint32_t iphase[2] = {0, 0};
     bool ok = true;
+    // Shared-memory descriptors of every operand buffer, built once; a K step
+    // adds its start-address offset (16-byte units) to the descriptor.
+    uint64_t dq[2], dp[2], dv[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      dq[i] = desc_kmajor_sw128(smem_addr(sm.qt[i]));
+      dp[i] = desc_kmajor_sw128(smem_addr(sm.pt[i]));
+      dv[i] = desc_mnmajor_sw128(smem_addr(sm.v[i]), kBox, 1024);
+    }
     auto issue_pv = [&](int u, bool acc) {
       const int pb = u & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
@@ -669,9 +678,10 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         return false;
       if (lane == 0) {
         tc_fence_after();
+        const uint64_t a0 = dv[pb], b0 = dp[pb];
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_f16_ss(tmem + 32, desc_mnmajor_sw128(smem_addr(sm.v[pb]) + ks * 2048, kBox, 1024),
-                     desc_kmajor_sw128(smem_addr(sm.pt[pb] + (ks >> 2) * kRowBox) + (ks & 3) * 32), kIdO,
+          mma_f16_ss(tmem + 32, a0 + (uint64_t)(ks * 128), b0 + (uint64_t)((ks >> 2) * 128 + (ks & 3) * 2), kIdO,
                      acc || ks > 0);
         mma_commit(&sm.p_free[pb]);
         mma_commit(&sm.v16empty[pb]);
@@ -695,11 +705,11 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         }
         if (lane == 0) {
           tc_fence_after();
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t koff = (ks & 3) * 32;
-            mma_f16_ts(tmem + sb * 16, tmem + kKCol + kb * 64 + ks * 8,
-                       desc_kmajor_sw128(smem_addr(sm.qt[slot] + (ks >> 2) * kRowBox) + koff), kIdS, ks > 0);
-          }
+          const uint64_t b0 = dq[slot];
+          const uint32_t a0 = tmem + kKCol + kb * 64, d = tmem + sb * 16;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_f16_ts(d, a0 + ks * 8, b0 + (uint64_t)((ks >> 2) * 128 + (ks & 3) * 2), kIdS, ks > 0);
           mma_commit(&sm.s_full[sb]);
           mma_commit(&sm.k16empty[kb]);
         }
@@ -729,7 +739,21 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     // Row of the tile this thread converts = its tensor-memory lane.
     const int ct = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
-    int slot = 0, u = 0;
+    // K of tile u is converted before V of tile u - 1, so S(u) can be
+    // issued while V(u - 1) is still being converted.
+    auto convert_v = [&](int uv) {
+      const int sv = uv % kNSV, vb = uv & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.vfull[sv], (uint32_t)(uv / kNSV) & 1u) &&
+                                       mbar_wait(&sm.v16empty[vb], ((uint32_t)(uv >> 1) & 1u) ^ 1u)) ||
+          aborted(sm))
+        return false;
+      convert_tile(sm.v8[sv], sm.v[vb], ct);
+      fence_async_smem();
+      mbar_arrive(&sm.v16full[vb]);
+      mbar_arrive(&sm.vempty[sv]);
+      return true;
+    };
+    int slot = 0, u = 0, uv = 0;   // tiles whose K / V are converted
     uint32_t iphase[2] = {0, 0};
     bool ok = true;
     while (ok) {
@@ -752,20 +776,20 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         tc_fence_before();
         mbar_arrive(&sm.k16full[kb]);
         mbar_arrive(&sm.kempty[st]);
-        const int sv = u % kNSV;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vfull[sv], (uint32_t)(u / kNSV) & 1u) &&
-                                         mbar_wait(&sm.v16empty[kb], ((uint32_t)(u >> 1) & 1u) ^ 1u)) ||
-            aborted(sm)) {
-          ok = false;
-          break;
+        if (uv < u) {
+          if (!convert_v(uv)) {
+            ok = false;
+            break;
+          }
+          ++uv;
         }
-        convert_tile(sm.v8[sv], sm.v[kb], ct);
-        fence_async_smem();
-        mbar_arrive(&sm.v16full[kb]);
-        mbar_arrive(&sm.vempty[sv]);
       }
       iphase[slot] ^= 1u;
       slot ^= 1;
+    }
+    while (ok && uv < u) {   // the last tile's V
+      if (!convert_v(uv)) ok = false;
+      ++uv;
     }
     if (!ok && lane == 0) set_abort(p, sm);
   } else {
