@@ -541,7 +541,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           mbar_arrive_tx(&sm.kfull[st], kTile);
           tma_load_2d(sm.k[st], &tmk, 0, row0 + t * kKT, &sm.kfull[st]);
           tma_load_2d(sm.k[st] + kBox, &tmk, 64, row0 + t * kKT, &sm.kfull[st]);
@@ -552,7 +552,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           mbar_arrive_tx(&sm.vfull[st], kTile);
           tma_load_2d(sm.v[st], &tmv, 0, row0 + t * kKT, &sm.vfull[st]);
           tma_load_2d(sm.v[st] + kBox, &tmv, 64, row0 + t * kKT, &sm.vfull[st]);
@@ -591,7 +591,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
                                        mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u)))
         return false;
-      if (lane == 0) {
+      if (elect_one()) {
         tc_fence_after();
         const uint64_t a0 = dv[st], b0 = dp[pb];
 #pragma unroll
@@ -618,7 +618,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           tc_fence_after();
           const uint64_t a0 = dk[st], b0 = dq[slot];
 #pragma unroll
@@ -633,7 +633,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       }
       if (ok && it.ntiles > 0 && !issue_pv(tau + it.ntiles - 1, it.ntiles > 1)) ok = false;
       if (!ok) break;
-      if (lane == 0) {
+      if (elect_one()) {
         mma_commit(&sm.o_full);
         mma_commit(&sm.iempty[slot]);
       }
@@ -644,7 +644,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
     }
     if (!ok && lane == 0) set_abort(p, sm);
-    if (lane == 0) {
+    if (elect_one()) {
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0);
     }

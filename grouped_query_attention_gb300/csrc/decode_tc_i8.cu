@@ -632,7 +632,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           mbar_arrive_tx(&sm.kfull[st], kTile8);
           tma_load_2d(sm.k8[st], &tmk, 0, row0 + t * kKT, &sm.kfull[st]);
         }
@@ -642,7 +642,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           mbar_arrive_tx(&sm.vfull[sv], kTile8);
           tma_load_2d(sm.v8[sv], &tmv, 0, row0 + t * kKT, &sm.vfull[sv]);
         }
@@ -676,7 +676,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
                                        mbar_wait(&sm.v16full[pb], (uint32_t)(u >> 1) & 1u)))
         return false;
-      if (lane == 0) {
+      if (elect_one()) {
         tc_fence_after();
         const uint64_t a0 = dv[pb], b0 = dp[pb];
 #pragma unroll
@@ -703,7 +703,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           tc_fence_after();
           const uint64_t b0 = dq[slot];
           const uint32_t a0 = tmem + kKCol + kb * 64, d = tmem + sb * 16;
@@ -718,7 +718,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       }
       if (ok && it.ntiles > 0 && !issue_pv(tau + it.ntiles - 1, it.ntiles > 1)) ok = false;
       if (!ok) break;
-      if (lane == 0) {
+      if (elect_one()) {
         mma_commit(&sm.o_full);
         mma_commit(&sm.iempty[slot]);
       }
@@ -729,7 +729,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
     }
     if (!ok && lane == 0) set_abort(p, sm);
-    if (lane == 0) {
+    if (elect_one()) {
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0);
     }

@@ -191,54 +191,70 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0) {
+    // The whole warp waits; one elected lane issues.
+    if (elect_one()) {
       mbar_arrive_tx(&sm.q_full, 2 * kTile);
       for (int q = 0; q < 2; ++q)
         for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.q[q] + bx * kBox, &tmq, bx * 64, qrow0 + q * kBM, &sm.q_full);
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kNS;
-        const uint32_t ph = (uint32_t)(t / kNS) & 1u;
-        if (!mbar_wait(&sm.kv_empty[st], ph ^ 1u) || aborted(sm)) {
-          set_abort(p, sm);
-          break;
-        }
-        const int row = krow0 + t * kBN;
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kNS;
+      const uint32_t ph = (uint32_t)(t / kNS) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[st], ph ^ 1u)) || aborted(sm)) {
+        if (lane == 0) set_abort(p, sm);
+        break;
+      }
+      const int row = krow0 + t * kBN;
+      if (elect_one()) {
         mbar_arrive_tx(&sm.k_full[st], kTile);
         for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.k[st] + bx * kBox, &tmk, bx * 64, row, &sm.k_full[st]);
         mbar_arrive_tx(&sm.v_full[st], kTile);
         for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.v[st] + bx * kBox, &tmv, bx * 64, row, &sm.v_full[st]);
-        issued = t + 1;
       }
-      // Drain: no copy of this CTA may still be landing when it exits.
-      mbar_wait(&sm.q_full, 0);
-      for (int t = max(0, issued - kNS); t < issued; ++t) {
-        mbar_wait(&sm.k_full[t % kNS], (uint32_t)(t / kNS) & 1u);
-        mbar_wait(&sm.v_full[t % kNS], (uint32_t)(t / kNS) & 1u);
-      }
+      __syncwarp();
+      issued = t + 1;
+    }
+    // Drain: no copy of this CTA may still be landing when it exits.
+    mbar_wait(&sm.q_full, 0);
+    for (int t = max(0, issued - kNS); t < issued; ++t) {
+      mbar_wait(&sm.k_full[t % kNS], (uint32_t)(t / kNS) & 1u);
+      mbar_wait(&sm.v_full[t % kNS], (uint32_t)(t / kNS) & 1u);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
+    // Shared-memory descriptors built once; a K step adds its start-address
+    // offset (16-byte units). One elected lane issues, the warp stays converged.
+    uint64_t dq[2], dk[kNS], dv[kNS];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) dq[i] = desc_kmajor_sw128(smem_addr(sm.q[i]));
+#pragma unroll
+    for (int i = 0; i < kNS; ++i) {
+      dk[i] = desc_kmajor_sw128(smem_addr(sm.k[i]));
+      dv[i] = desc_mnmajor_sw128(smem_addr(sm.v[i]), kBox, 1024);
+    }
     auto issue_s = [&](int q, int st) {
       const uint32_t d = tmem + q * 128;
+      const uint64_t a0 = dq[q], b0 = dk[st];
+#pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks & 3) * 32;
-        mma_f16_ss(d, desc_kmajor_sw128(smem_addr(sm.q[q] + (ks >> 2) * kBox) + koff),
-                   desc_kmajor_sw128(smem_addr(sm.k[st] + (ks >> 2) * kBox) + koff), kIdS, ks > 0);
+        const uint64_t off = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
+        mma_f16_ss(d, a0 + off, b0 + off, kIdS, ks > 0);
       }
       mma_commit(&sm.s_full[q]);
     };
     auto issue_pv = [&](int q, int st, bool acc) {
       const uint32_t d = tmem + 256 + q * 128;
       const uint32_t pa = tmem + q * 128;  // P over the first 64 columns of S_q
-      for (int ks = 0; ks < 8; ++ks)
-        mma_f16_ts(d, pa + ks * 8, desc_mnmajor_sw128(smem_addr(sm.v[st]) + ks * 2048, kBox, 1024), kIdO,
-                   acc || ks > 0);
+      const uint64_t b0 = dv[st];
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) mma_f16_ts(d, pa + ks * 8, b0 + (uint64_t)(ks * 128), kIdO, acc || ks > 0);
       mma_commit(&sm.o_done[q]);
     };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.k_full[0], 0));
     if (ok) {
-      if (lane == 0) {
+      if (elect_one()) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(1, 0);
@@ -266,7 +282,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           tc_fence_after();
           issue_pv(0, st, t > 0);
         }
@@ -277,13 +293,13 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           ok = false;
           break;
         }
-        if (more && lane == 0) issue_s(0, st1);
+        if (more && elect_one()) issue_s(0, st1);
         __syncwarp();
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[1], tp))) {
           ok = false;
           break;
         }
-        if (lane == 0) {
+        if (elect_one()) {
           tc_fence_after();
           issue_pv(1, st, t > 0);
           mma_commit(&sm.kv_empty[st]);
@@ -295,7 +311,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     }
     if (!ok && lane == 0) set_abort(p, sm);
     // Drain: every MMA this thread issued has finished before tensor memory is freed.
-    if (lane == 0) {
+    if (elect_one()) {
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0);
     }

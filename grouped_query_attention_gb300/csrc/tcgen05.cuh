@@ -54,6 +54,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 
+// One elected lane of a converged warp (elect.sync: the same lane each time
+// for the same full mask), so the issuing code stays on the warp-uniform path.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{ .reg .pred p; elect.sync _|p, 0xffffffff; selp.u32 %0, 1, 0, p; }" : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 
 // 2D tiled tensor load: box at (c0 = innermost coordinate, c1) into dst.
