@@ -90,6 +90,16 @@ struct __align__(1024) DSmem {
 
 __device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoft) : "memory"); }
 
+// Named barrier of the softmax threads that also returns the OR of `v` over them.
+__device__ __forceinline__ bool named_sync_or(bool v) {
+  uint32_t r;
+  asm volatile("{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, 1, %2, q; selp.u32 %0, 1, 0, p; }"
+               : "=r"(r)
+               : "r"((uint32_t)v), "n"(kSoft)
+               : "memory");
+  return r != 0;
+}
+
 // Merge ticket with acquire-release ordering at GPU scope: after the named
 // barrier, the release covers every softmax thread's partial stores, and the
 // acquire makes the other splits' partials visible to the last one.
@@ -526,8 +536,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       mbar_init(&sm.iready[s], 1);
       mbar_init(&sm.iempty[s], 2);  // MMA commit (Q^T reads done) + softmax release
       mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.s_free[s], kSoft);
-      mbar_init(&sm.p_full[s], kSoft);
+      mbar_init(&sm.s_free[s], kSoft / 32);   // one arrival per softmax warp
+      mbar_init(&sm.p_full[s], kSoft / 32);
       mbar_init(&sm.p_free[s], 1);
     }
     mbar_init(&sm.o_full, 1);
@@ -832,6 +842,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         const int jk = it.j0 + t * kKT + kl;      // this thread's key
         const bool key_ok = jk < it.jend;
         float s[R];
+        bool grow_here = false;   // a visible score exceeds its row's reference by more than 2^kLazy
         bool got = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (uint32_t)(u >> 1) & 1u));
         if (got) {
           tc_fence_after();
@@ -839,7 +850,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           tmem_ld16(tmem + lane_addr + sb * 16, raw);
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&sm.s_free[sb]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.s_free[sb]);
           // (V rows past the key range hold int8 codes, finite, and get P = 0.)
 #pragma unroll
           for (int r = 0; r < R; ++r) {
@@ -855,27 +867,35 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
                       p.bias_ld + jk;
               x += load_t(p.bias, bi, p.t_type) * kLog2e;
             }
-            s[r] = vis ? x : kNegBig;
+            s[r] = vis ? x : -INFINITY;
+            grow_here = grow_here || s[r] > m_run[r] + kLazy;
+          }
+        } else if (lane == 0) {
+          set_abort(p, sm);
+        }
+        // One barrier tells every softmax thread whether any row needs a new
+        // reference max (rare after an item's first tile).
+        const bool any_grow = named_sync_or(grow_here);
+        if (aborted(sm)) {
+          bad = true;
+          break;
+        }
+        float mt[R];
+        if (any_grow) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
             float m = s[r];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
             if (lane == 0) sm.red[sb][ws][r] = m;
           }
-        } else if (lane == 0) {
-          set_abort(p, sm);
-        }
-        named_sync();
-        if (aborted(sm)) {
-          bad = true;
-          break;
-        }
-        // Tile max per row; lazy rescale of O^T (only after the item's first tile).
-        float mt[R];
-        bool any_grow = false;
+          named_sync();
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          mt[r] = fmaxf(fmaxf(sm.red[sb][0][r], sm.red[sb][1][r]), fmaxf(sm.red[sb][2][r], sm.red[sb][3][r]));
-          any_grow = any_grow || mt[r] > m_run[r] + kLazy;
+          for (int r = 0; r < R; ++r)
+            mt[r] = fmaxf(fmaxf(sm.red[sb][0][r], sm.red[sb][1][r]), fmaxf(sm.red[sb][2][r], sm.red[sb][3][r]));
+        } else {
+#pragma unroll
+          for (int r = 0; r < R; ++r) mt[r] = m_run[r];
         }
         if (any_grow && t > 0) {
           // O^T must hold P.V up to tile t-1.
@@ -907,7 +927,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            const float pr = s[r] <= kNegBig ? 0.f : ex2(s[r] - m_run[r]);
+            const float pr = ex2(s[r] - m_run[r]);   // masked scores are -inf: 0
             l_part[r] += pr;
             const __half ph = __float2half_rn(pr);
             *reinterpret_cast<__half*>(sm.pt[sb] + sw_elem(r, kl, kRowBox)) = ph;
@@ -919,7 +939,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         }
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(&sm.p_full[sb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[sb]);
       }
       if (bad) break;
       tau += it.ntiles;
