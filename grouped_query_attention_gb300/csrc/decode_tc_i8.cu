@@ -37,7 +37,7 @@ using namespace tc;
 constexpr int kHD = 128;
 constexpr int kKT = kTcDecodeTile;       // keys per tile (128)
 constexpr int kNR = 16;                  // MMA N: hi and lo query rows of the group, padded
-constexpr int kNS = 4;                   // int8 K stages
+constexpr int kNS = 5;                   // int8 K stages
 constexpr int kNSV = 4;                  // int8 V stages
 constexpr int kThreads = 352;            // TMA, MMA, preparer, 4 softmax, 4 converter warps
 constexpr int kSoftWarp0 = 3;            // first softmax warp
