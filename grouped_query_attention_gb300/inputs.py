@@ -61,7 +61,8 @@ class CaseSpec:
     smooth_softmax: int = -1
     bias: tuple | None = None          # (batch_dim, head_dim, std): dims are B or 1, N or 1
     scale: float = 0.0
-    quant: str = "NONE"                # NONE | PER_TENSOR | PER_CHANNEL (int8 cache)
+    quant: str = "NONE"                # NONE | PER_TENSOR | PER_CHANNEL (quantised cache)
+    bits: int = 8                      # 8: int8 codes; 4: two 4-bit codes per byte (prompt only)
     scale_range: tuple = (0.005, 0.02)
     extra: dict = field(default_factory=dict)
 
@@ -105,7 +106,8 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
     T = NP_DTYPE[spec.dtype]
     B, S, N, Nkv, H = spec.B, spec.S, spec.N, spec.Nkv, spec.H
     quant = spec.quant != "NONE"
-    cache_dtype = np.int8 if quant else T
+    int4 = quant and spec.bits == 4
+    cache_dtype = (np.uint8 if int4 else np.int8) if quant else T
     seqlens = draw_seqlens(spec, seed)
     if seqlens.shape != (B,):
         raise ValueError("seqlens_k must give one value per batch")
@@ -119,8 +121,10 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
     inp["total_sequence_length"] = np.array([total_len], dtype=np.int32)
 
     def cache(name, length):
-        shape = (B, Nkv, length, H)
         rng = _rng(seed, name)
+        if int4:   # packed bytes: any bit pattern is a valid pair of codes
+            return rng.integers(0, 256, size=(B, Nkv, length, H // 2), dtype=np.int16).astype(np.uint8)
+        shape = (B, Nkv, length, H)
         return _int8_uniform(rng, shape) if quant else _normal(rng, shape, cache_dtype)
 
     share = spec.mode == "shared"
@@ -160,7 +164,7 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
                  do_rotary=1 if spec.rotary_theta is not None else 0,
                  local_window_size=spec.local_window_size, scale=spec.scale, softcap=spec.softcap,
                  qk_norm_epsilon=spec.qk_norm_epsilon, smooth_softmax=spec.smooth_softmax,
-                 k_quant_type=spec.quant, v_quant_type=spec.quant, kv_cache_bit_width=8,
+                 k_quant_type=spec.quant, v_quant_type=spec.quant, kv_cache_bit_width=spec.bits,
                  sliding_window_cache=0)
     return dict(inputs=inp, attrs=attrs, present_key=present_k, present_value=present_v,
                 share_buffer=share, spec=spec)

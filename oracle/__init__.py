@@ -24,8 +24,11 @@ from .gqa import (  # noqa: F401
     DEFAULT_ATTRS,
     dequantize_int8,
     gqa_forward,
+    pack_int4,
+    quantize_int4,
     quantize_int8,
     rms_norm,
     rotary_neox,
     softcap_scores,
+    unpack_int4,
 )

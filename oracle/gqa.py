@@ -18,6 +18,9 @@ the readings the library implements):
     logit that enters only the softmax denominator;
   * int8 code = clamp(round_half_even(fp32(x) / fp32(scale)), -127, 127),
     the division done in IEEE fp32, dequantised as code * scale;
+  * int4 (kv_cache_bit_width = 4) code = clamp(round_half_even(fp32(x) /
+    fp32(scale)), -7, 7), stored as the nibble code + 8, two per byte with
+    the even coordinate in the low nibble; only prompts (no past cache);
   * RMS norm y = x / sqrt(mean(x^2) + eps) * w, weight used as given;
   * padding rows of a prompt (i >= total_b, no past) produce a zero output row;
     their K/V rows are still appended.
@@ -123,17 +126,56 @@ def dequantize_int8(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return np.asarray(q, dtype=np.float64) * np.asarray(scale, dtype=np.float64)
 
 
-def _store(x64: np.ndarray, cache_dtype, quant_type: str, scale, g: int, head_size: int) -> np.ndarray:
-    """Value written into the present cache for one new row (round to nearest, or int8 code)."""
+def quantize_int4(x: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """Symmetric 4-bit code of fp32 values: clamp(rint(fp32(x) / scale), -7, 7) (int8 array).
+
+    Same rounding as the int8 code (IEEE fp32 division, ties to even) with the
+    symmetric 4-bit range. com.microsoft.GroupQueryAttention, section
+    Attributes (kv_cache_bit_width = 4) and section Implementation variants
+    (quant_int4_flash_prefill builds a 4-bit cache).
+    """
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    t = x32 / np.asarray(scale, dtype=np.float32)
+    return np.clip(np.rint(t), -7, 7).astype(np.int8)
+
+
+def pack_int4(codes: np.ndarray) -> np.ndarray:
+    """Codes (..., H) in [-8, 7] as bytes (..., H/2): nibble = code + 8, coordinate
+    2k in the low nibble of byte k and 2k+1 in the high nibble.
+
+    com.microsoft.GroupQueryAttention, section Attributes (kv_cache_bit_width:
+    "four-bit values are packed two per uint8 element").
+    """
+    n = (np.asarray(codes, dtype=np.int16) + 8).astype(np.uint8)
+    return (n[..., 0::2] | (n[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(packed: np.ndarray) -> np.ndarray:
+    """Inverse of pack_int4: bytes (..., H/2) to codes (..., H) in [-8, 7]."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = (b & 0x0F).astype(np.int16) - 8
+    out[..., 1::2] = (b >> 4).astype(np.int16) - 8
+    return out
+
+
+def _store(x64: np.ndarray, cache_dtype, quant_type: str, scale, g: int, head_size: int,
+           bits: int = 8) -> np.ndarray:
+    """Value written into the present cache for one new row (round to nearest, or an int8 / packed int4 code)."""
     if quant_type != "NONE":
-        return quantize_int8(x64, _scale_vector(scale, quant_type, g, head_size))
+        sv = _scale_vector(scale, quant_type, g, head_size)
+        if bits == 4:
+            return pack_int4(quantize_int4(x64, sv))
+        return quantize_int8(x64, sv)
     return np.asarray(x64, dtype=np.float64).astype(cache_dtype)
 
 
-def _load(rows: np.ndarray, quant_type: str, scale, g: int, head_size: int) -> np.ndarray:
-    """fp64 values of cached rows as attention reads them (dequantised if int8)."""
+def _load(rows: np.ndarray, quant_type: str, scale, g: int, head_size: int, bits: int = 8) -> np.ndarray:
+    """fp64 values of cached rows as attention reads them (dequantised if quantised)."""
     if quant_type != "NONE":
-        return dequantize_int8(rows, _scale_vector(scale, quant_type, g, head_size))
+        sv = _scale_vector(scale, quant_type, g, head_size)
+        codes = unpack_int4(rows) if bits == 4 else rows
+        return dequantize_int8(codes, sv)
     return np.asarray(rows, dtype=np.float64)
 
 
@@ -198,6 +240,9 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
     seqlens = np.asarray(inputs["seqlens_k"], dtype=np.int64).reshape(-1)
     total_len = int(np.asarray(inputs["total_sequence_length"]).reshape(-1)[0])
     kq, vq = a["k_quant_type"], a["v_quant_type"]
+    bits = int(a["kv_cache_bit_width"])
+    if kq != "NONE" and bits == 4 and has_past:
+        raise ValueError("a 4-bit cache is built by a prompt (no past cache)")
     k_scale, v_scale = inputs.get("k_scale"), inputs.get("v_scale")
     qw, kw = inputs.get("q_norm_weight"), inputs.get("k_norm_weight")
     if (qw is None) != (kw is None):
@@ -244,8 +289,8 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 kr = rms_norm(kr, kw, eps)
             if rotary:
                 kr = rotary_neox(kr, cos_c[pos], sin_c[pos])
-            pk[b, g, pos] = _store(kr, pk.dtype, kq, k_scale, g, H)
-            pv[b, g, pos] = _store(vr, pv.dtype, vq, v_scale, g, H)
+            pk[b, g, pos] = _store(kr, pk.dtype, kq, k_scale, g, H, bits)
+            pv[b, g, pos] = _store(vr, pv.dtype, vq, v_scale, g, H, bits)
             new_k[b, g], new_v[b, g] = kr, vr
         new_pos[b] = pos
 
@@ -261,8 +306,8 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 if rows.size == 0:
                     continue
             g = h // G if head_of_group == "block" else h % Nkv
-            kd = _load(pk[b, g, :total_b], kq, k_scale, g, H)
-            vd = _load(pv[b, g, :total_b], vq, v_scale, g, H)
+            kd = _load(pk[b, g, :total_b], kq, k_scale, g, H, bits)
+            vd = _load(pv[b, g, :total_b], vq, v_scale, g, H, bits)
             qr = q_in[b, rows, h * H:(h + 1) * H].astype(np.float64)
             if qw is not None:
                 qr = rms_norm(qr, qw, eps)

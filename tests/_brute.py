@@ -36,6 +36,8 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
         pv = [[[r.copy() for r in present_value[b, g]] for g in range(Nkv)] for b in range(B)]
         cache_dtype = present_key.dtype
     quant = attrs.get("k_quant_type", "NONE") != "NONE"
+    int4 = quant and attrs.get("kv_cache_bit_width", 8) == 4
+    qmax = 7 if int4 else 127
     eps = attrs.get("qk_norm_epsilon", 1e-6)
     qw = inputs.get("q_norm_weight")
     kw = inputs.get("k_norm_weight")
@@ -73,13 +75,21 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
             for d in range(H):
                 s32 = sc[0] if sc.size == 1 else sc[g * H + d]
                 t = np.float32(vec[d]) / np.float32(s32)
-                codes.append(max(-127, min(127, round(float(t)))))   # Python round: ties to even
+                codes.append(max(-qmax, min(qmax, round(float(t)))))   # Python round: ties to even
+            if int4:   # byte k = biased code of 2k + 16 * biased code of 2k+1
+                return np.array([(codes[2 * k] + 8) + 16 * (codes[2 * k + 1] + 8) for k in range(H // 2)],
+                                dtype=np.uint8)
             return np.array(codes, dtype=np.int8)
         return np.array(vec, dtype=np.float64).astype(cache_dtype)
 
     def value(row, g, name):
         if quant:
             sc = scales(name, g)
+            if int4:
+                codes = []
+                for byte in row:
+                    codes += [int(byte) % 16 - 8, int(byte) // 16 - 8]
+                return [codes[d] * sc[d] for d in range(H)]
             return [int(row[d]) * sc[d] for d in range(H)]
         return [_f(x) for x in row]
 

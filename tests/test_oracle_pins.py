@@ -51,6 +51,10 @@ BRUTE_CASES = {
     "f16_mha": tiny(dtype="f16", N=2, Nkv=2, mode="shared", S=2, capacity=6, seqlens_k=(3, 5)),
     "bidirectional": tiny(causal=0, seqlens_k=(2, 2)),
     "explicit_scale_g4": tiny(N=8, Nkv=2, scale=0.3, mode="shared", S=1, capacity=5, seqlens_k=(2, 4)),
+    "int4_per_channel_prompt": tiny(S=4, capacity=6, seqlens_k=(3, 2), quant="PER_CHANNEL", bits=4,
+                                    scale_range=(0.15, 0.4)),
+    "int4_per_tensor_norm_rotary": tiny(S=3, capacity=5, seqlens_k=(2, 2), quant="PER_TENSOR", bits=4,
+                                        qk_norm=True, rotary_theta=1e4, scale_range=(0.2, 0.3)),
 }
 
 
@@ -63,7 +67,7 @@ def test_brute_force_matches(name):
     np.testing.assert_allclose(res["output_f64"], out_b, rtol=1e-11, atol=1e-12)
     for got, want in ((res["present_key"], pk_b), (res["present_value"], pv_b)):
         assert got.dtype == want.dtype
-        if got.dtype == np.int8:
+        if got.dtype in (np.int8, np.uint8):
             assert np.array_equal(got, want)
         else:
             np.testing.assert_allclose(got.astype(np.float64), want.astype(np.float64), rtol=2e-7, atol=0)
@@ -375,6 +379,51 @@ def test_int8_per_channel_scale_index():
     inp["key"][0, 0] = np.arange(1, 17, dtype=np.float32) / 64 * 3
     res = run(case)
     assert np.all(res["present_key"][0, :, 1] == 3)
+
+
+# ---------------------------------------------------------------- int4 quantisation and packing
+
+def test_int4_pack_layout_worked_example():
+    """+8-biased nibbles, even head coordinate low (com.microsoft.GroupQueryAttention, section Inputs)."""
+    codes = np.array([-7, 7, 0, 1, -8, 3], dtype=np.int8)
+    # byte 0: low nibble -7+8 = 0x1, high 7+8 = 0xF; byte 1: 0x8 | 0x9 << 4; byte 2: 0x0 | 0xB << 4
+    assert list(oracle.pack_int4(codes)) == [0xF1, 0x98, 0xB0]
+    every = np.arange(256, dtype=np.uint8)
+    assert np.array_equal(oracle.pack_int4(oracle.unpack_int4(every)), every)
+    u = oracle.unpack_int4(every)
+    assert u.min() == -8 and u.max() == 7 and list(u[:4]) == [-8, -8, -7, -8]
+
+
+def test_int4_round_trip_error_bound_saturation_ties():
+    scale = np.float32(0.25)
+    codes = np.arange(-7, 8)
+    vals = (codes * np.float64(scale)).astype(np.float32)
+    assert np.array_equal(oracle.quantize_int4(vals, scale), codes.astype(np.int8))
+    x = np.random.default_rng(6).uniform(-1.75, 1.75, 4096).astype(np.float32)
+    q = oracle.quantize_int4(x, scale)
+    assert np.all(np.abs(x - q * np.float64(scale)) <= scale / 2 * (1 + 1e-6))
+    assert oracle.quantize_int4(np.float32(9.0), scale) == 7
+    assert oracle.quantize_int4(np.float32(-9.0), scale) == -7      # symmetric: never -8
+    s1 = np.float32(1.0)
+    assert list(oracle.quantize_int4(np.array([2.5, 3.5, -2.5, 0.5, 6.5], np.float32), s1)) == [2, 4, -2, 0, 6]
+
+
+def test_int4_prompt_cache_bytes_and_rejects_past():
+    """A prompt writes packed codes of K/V into present rows [0, S); a past cache is rejected."""
+    spec = tiny(B=1, S=2, N=2, Nkv=1, H=4, capacity=3, seqlens_k=(1,), quant="PER_TENSOR", bits=4)
+    case = generate(spec, seed=21)
+    inp = case["inputs"]
+    inp["k_scale"][:] = 0.5
+    inp["key"][0] = np.array([[1.0, -1.0, 3.5, -3.5], [0.25, 0.75, 9.0, -0.2]], np.float32)
+    res = run(case)
+    # codes [2,-2,7,-7] -> nibbles [10,6,15,1]; [0,2,7,0] -> nibbles [8,10,15,8] (0.25/0.5 ties to 0)
+    assert list(res["present_key"][0, 0, 0]) == [10 | 6 << 4, 15 | 1 << 4]
+    assert list(res["present_key"][0, 0, 1]) == [8 | 10 << 4, 15 | 8 << 4]
+    assert np.array_equal(res["present_key"][0, 0, 2], case["present_key"][0, 0, 2])
+    shared = generate(tiny(mode="shared", S=1, capacity=4, seqlens_k=(2, 3), quant="PER_TENSOR", bits=4),
+                      seed=21)
+    with pytest.raises(ValueError):
+        run(shared)
 
 
 # ---------------------------------------------------------------- cache bookkeeping
