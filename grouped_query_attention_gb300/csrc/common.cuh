@@ -4,6 +4,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "gqa_internal.h"
 
 namespace gqa {
@@ -62,6 +64,16 @@ __device__ __forceinline__ int8_t quant_i8(float x, float s) {
   t = rintf(t);
   t = fminf(fmaxf(t, -127.0f), 127.0f);
   return static_cast<int8_t>(static_cast<int>(t));
+}
+
+// 4-bit cache code as its stored nibble: clamp(rint(x / s), -7, 7) + 8, the
+// division in IEEE fp32 (com.microsoft.GroupQueryAttention, section Inputs:
+// +8-biased nibbles; section Attributes: kv_cache_bit_width).
+__device__ __forceinline__ unsigned quant_i4_nibble(float x, float s) {
+  float t = __fdiv_rn(x, s);
+  t = rintf(t);
+  t = fminf(fmaxf(t, -7.0f), 7.0f);
+  return static_cast<unsigned>(static_cast<int>(t) + 8);
 }
 
 __device__ __forceinline__ float channel_scale(const float* sc, int n, int c) {

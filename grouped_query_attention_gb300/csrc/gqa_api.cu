@@ -122,19 +122,24 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   const gqa_tensor& pv = out->present_value;
   if (!present(pk) || !present(pv)) return fail(GQA_ERR_INVALID_ARGUMENT, "present_key and present_value are required");
   int cache_dt = q.dtype;
+  bool i4 = false;   // 4-bit cache: uint8 rows of head_size/2 bytes, two +8-biased nibbles each
   if (kq) {
     if (q.dtype != GQA_F32) return fail(GQA_ERR_INVALID_ARGUMENT, "a quantised cache requires float32 query/key/value/output");
-    if (a.kv_cache_bit_width == 4 || pk.dtype == GQA_U8) return fail(GQA_ERR_UNSUPPORTED, "int4 cache is not implemented");
-    if (a.kv_cache_bit_width != 8) return fail(GQA_ERR_INVALID_ARGUMENT, "kv_cache_bit_width must be 8 or 4");
-    cache_dt = GQA_I8;
+    if (a.kv_cache_bit_width != 8 && a.kv_cache_bit_width != 4)
+      return fail(GQA_ERR_INVALID_ARGUMENT, "kv_cache_bit_width must be 8 or 4");
+    i4 = a.kv_cache_bit_width == 4;
+    cache_dt = i4 ? GQA_U8 : GQA_I8;
   }
   if (pk.dtype != cache_dt || pv.dtype != cache_dt) {
     if (!kq && (pk.dtype == GQA_F32 || pk.dtype == GQA_F16))
       return fail(GQA_ERR_UNSUPPORTED, "a float cache of another dtype than query is not implemented");
-    return fail(GQA_ERR_INVALID_ARGUMENT, "present cache dtype must be %s", kq ? "int8" : "the query dtype");
+    return fail(GQA_ERR_INVALID_ARGUMENT, "present cache dtype must be %s",
+                i4 ? "uint8 (packed 4-bit codes)" : kq ? "int8" : "the query dtype");
   }
-  if (pk.ndim != 4 || pk.shape[0] != B || pk.shape[1] != Nkv || pk.shape[3] != H)
-    return fail(GQA_ERR_INVALID_ARGUMENT, "present_key must be (B, kv_num_heads, C, head_size), got %s", shape_str(pk).c_str());
+  const long long row_w = i4 ? H / 2 : H;   // cache elements per row
+  if (pk.ndim != 4 || pk.shape[0] != B || pk.shape[1] != Nkv || pk.shape[3] != row_w)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "present_key must be (B, kv_num_heads, C, %s), got %s",
+                i4 ? "head_size/2" : "head_size", shape_str(pk).c_str());
   if (!shape_is(pv, 4, pk.shape))
     return fail(GQA_ERR_INVALID_ARGUMENT, "present_value shape must equal present_key shape");
   const long long C = pk.shape[2];
@@ -144,6 +149,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   if (has_pk != has_pv) return fail(GQA_ERR_INVALID_ARGUMENT, "past_key and past_value come together");
   int mode = gqa::kPrompt;
   long long past_cap = 0;
+  if (has_pk && i4) return fail(GQA_ERR_UNSUPPORTED, "a 4-bit cache is prompt-only: past_key/past_value are not accepted");
   if (has_pk) {
     const gqa_tensor& qk = in->past_key;
     const gqa_tensor& qv = in->past_value;
@@ -257,7 +263,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.B = (int)B; P.S = (int)S; P.N = N; P.Nkv = Nkv; P.G = G; P.H = (int)H;
   P.C = (int)C; P.past_cap = (int)past_cap; P.total_len = (int)T; P.mode = mode;
   P.t_type = tdt == GQA_F16 ? gqa::kF16 : gqa::kF32;
-  P.cache_type = kq ? gqa::kI8 : P.t_type;
+  P.cache_type = i4 ? gqa::kI4 : kq ? gqa::kI8 : P.t_type;
   P.k_quant = a.k_quant_type; P.v_quant = a.v_quant_type;
   P.causal = a.causal ? 1 : 0;
   P.window = a.local_window_size;
@@ -272,7 +278,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.out = out->output.data;
 
   // ---- regime and workspace plan
-  pl->decode = gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P));
+  // A 4-bit cache is built by a prompt and always takes the prefill kernels.
+  pl->decode = !i4 && (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P)));
   pl->tc_i8 = pl->decode && gqa::decode_tc_i8_supported(P);
   pl->tc_decode = pl->decode && (gqa::decode_tc_supported(P) || pl->tc_i8);
   pl->tensor_core = false;
@@ -388,8 +395,8 @@ gqa_status gqa_create(const gqa_attrs* a, gqa_handle** out) {
   for (int qt : {a->k_quant_type, a->v_quant_type})
     if (qt < GQA_QUANT_NONE || qt > GQA_QUANT_PER_CHANNEL) return fail(GQA_ERR_INVALID_ARGUMENT, "unknown quant type %d", qt);
   if (a->sliding_window_cache == 1) return fail(GQA_ERR_UNSUPPORTED, "sliding_window_cache is not implemented");
-  if ((a->k_quant_type != GQA_QUANT_NONE) && a->kv_cache_bit_width == 4)
-    return fail(GQA_ERR_UNSUPPORTED, "int4 cache is not implemented");
+  if (a->k_quant_type != GQA_QUANT_NONE && a->kv_cache_bit_width != 8 && a->kv_cache_bit_width != 4)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "kv_cache_bit_width must be 8 or 4");
   gqa_handle* h = new (std::nothrow) gqa_handle;
   if (!h) return fail(GQA_ERR_INVALID_ARGUMENT, "out of host memory");
   h->attrs = *a;

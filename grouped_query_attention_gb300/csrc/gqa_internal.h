@@ -9,7 +9,7 @@
 namespace gqa {
 
 enum CacheMode : int { kPrompt = 0, kShared = 1, kCopy = 2 };
-enum ElemType : int { kF32 = 1, kF16 = 2, kI8 = 3 };
+enum ElemType : int { kF32 = 1, kF16 = 2, kI8 = 3, kI4 = 4 };  // kI4: two +8-biased nibbles per byte
 
 // Everything a kernel needs about one gqa_forward call. Passed by value as a
 // kernel parameter (well under the 32 KB parameter limit).
@@ -21,7 +21,7 @@ struct Params {
   int total_len;  // total_sequence_length (host scalar)
   int mode;       // CacheMode
   int t_type;     // ElemType of query/key/value/output (kF32 | kF16)
-  int cache_type; // ElemType of the cache (kF32 | kF16 | kI8)
+  int cache_type; // ElemType of the cache (kF32 | kF16 | kI8 | kI4)
   int k_quant, v_quant;  // gqa_quant values
   // ---- attributes (resolved)
   int causal;

@@ -1,11 +1,12 @@
 // CUDA-core flash prefill for GroupQueryAttention: float32 Q/K/V (including
-// an int8 cache read back through its scales) and head sizes the tensor-core
-// kernel does not take. Reads the prepared queries the pre-pass left in the
+// an int8 or 4-bit cache read back through its scales) and head sizes the
+// tensor-core kernel does not take. Reads the prepared queries the pre-pass left in the
 // workspace and the present cache after the append.
 //
 // com.microsoft.GroupQueryAttention, section Implementation variants
 // (qkv_present_flash_cluster / past_kv_flash_prefill / new_kv_past_flash_prefill
-// / quant_int8_flash_prefill: online-softmax prefill over the cache as stored,
+// / quant_int8_flash_prefill / quant_int4_flash_prefill: online-softmax
+// prefill over the cache as stored,
 // causal bound right-aligned at the live length, window floor, softcap, bias
 // and head sink) and sections Inputs / Attributes.
 //
@@ -69,9 +70,12 @@ prefill_simt_kernel(const Params p) {
 #pragma unroll
     for (int e = 0; e < kMaxH / 32; ++e) o[rr][e] = 0.f;
   }
-  const CacheT* kb = reinterpret_cast<const CacheT*>(p.present_k) + ((long long)b * p.Nkv + g) * p.C * H;
-  const CacheT* vb = reinterpret_cast<const CacheT*>(p.present_v) + ((long long)b * p.Nkv + g) * p.C * H;
-  const bool i8 = sizeof(CacheT) == 1;
+  // CacheT = uint8_t: 4-bit cache, H/2 bytes per row (+8-biased nibbles, even coordinate low).
+  constexpr bool i4 = std::is_same<CacheT, uint8_t>::value;
+  constexpr bool i8 = std::is_same<CacheT, int8_t>::value;
+  const long long row_elems = i4 ? H / 2 : H;
+  const CacheT* kb = reinterpret_cast<const CacheT*>(p.present_k) + ((long long)b * p.Nkv + g) * p.C * row_elems;
+  const CacheT* vb = reinterpret_cast<const CacheT*>(p.present_v) + ((long long)b * p.Nkv + g) * p.C * row_elems;
 
   for (int t0 = kmin; t0 < kmax; t0 += kTile) {
     __syncthreads();
@@ -80,7 +84,14 @@ prefill_simt_kernel(const Params p) {
       float kv = 0.f, vv = 0.f;
       if (t0 + j < kmax) {
         const long long idx = (long long)(t0 + j) * H + d;
-        if (i8) {
+        if constexpr (i4) {
+          const long long bi = (long long)(t0 + j) * (H / 2) + (d >> 1);
+          const int sh = (d & 1) * 4;
+          const int kc = (int)((reinterpret_cast<const uint8_t*>(kb)[bi] >> sh) & 15) - 8;
+          const int vc = (int)((reinterpret_cast<const uint8_t*>(vb)[bi] >> sh) & 15) - 8;
+          kv = (float)kc * channel_scale(p.k_scale, p.k_scale_n, g * H + d);
+          vv = (float)vc * channel_scale(p.v_scale, p.v_scale_n, g * H + d);
+        } else if (i8) {
           kv = (float)reinterpret_cast<const int8_t*>(kb)[idx] * channel_scale(p.k_scale, p.k_scale_n, g * H + d);
           vv = (float)reinterpret_cast<const int8_t*>(vb)[idx] * channel_scale(p.v_scale, p.v_scale_n, g * H + d);
         } else if (sizeof(CacheT) == 2) {
@@ -183,6 +194,10 @@ cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st) {
     e = cudaFuncSetAttribute(prefill_simt_kernel<float, int8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prefill_simt_kernel<float, int8_t><<<grid, block, smem, st>>>(p);
+  } else if (p.cache_type == kI4) {
+    e = cudaFuncSetAttribute(prefill_simt_kernel<float, uint8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prefill_simt_kernel<float, uint8_t><<<grid, block, smem, st>>>(p);
   } else {
     e = cudaFuncSetAttribute(prefill_simt_kernel<float, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

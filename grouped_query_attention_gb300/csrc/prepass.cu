@@ -1,5 +1,6 @@
 // Pre-pass of the prefill path: appends the new K/V rows to the present cache
-// (RMS norm -> NeoX rotary -> cast or int8 code for K; cast or code for V) and
+// (RMS norm -> NeoX rotary -> cast, int8 code or packed 4-bit code for K;
+// the same store for V) and
 // writes the prepared queries (norm -> rotary) to the workspace for the
 // attention kernel. One warp per row, 16-byte vector loads and stores.
 //
@@ -69,8 +70,43 @@ __device__ __forceinline__ void store_n(DstT* dst, const float* src) {
 // Row roles of the flattened row index.
 enum Role { kKey = 0, kValue = 1, kQuery = 2 };
 
+// Appends V consecutive values (head coordinates d0 .. d0+V-1 of row pos of KV
+// head `head`) to the present K or V cache: a cast for a float cache, int8
+// codes, or for a 4-bit cache (CacheT = uint8_t) V/2 bytes of +8-biased
+// nibbles with the even coordinate in the low nibble.
+template <typename CacheT, int V>
+__device__ __forceinline__ void append_chunk(const Params& p, int role, int b, int head, int pos, int d0,
+                                             const float* y) {
+  const int H = p.H;
+  const long long row = ((long long)b * p.Nkv + head) * p.C + pos;
+  void* base = role == kKey ? p.present_k : p.present_v;
+  if constexpr (std::is_same<CacheT, uint8_t>::value) {
+    static_assert(V == 4, "4-bit cache: fp32 rows, four values per chunk");
+    const float* sc = role == kKey ? p.k_scale : p.v_scale;
+    const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
+    unsigned n[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) n[k] = quant_i4_nibble(y[k], channel_scale(sc, nsc, head * H + d0 + k));
+    const unsigned short packed = (unsigned short)(n[0] | (n[1] << 4) | (n[2] << 8) | (n[3] << 12));
+    *reinterpret_cast<unsigned short*>(reinterpret_cast<uint8_t*>(base) + row * (H / 2) + d0 / 2) = packed;
+  } else if constexpr (sizeof(CacheT) == 1) {
+    const float* sc = role == kKey ? p.k_scale : p.v_scale;
+    const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
+    char4 q4[V / 4];
+    int8_t* qb = reinterpret_cast<int8_t*>(q4);
+#pragma unroll
+    for (int k = 0; k < V; ++k) qb[k] = quant_i8(y[k], channel_scale(sc, nsc, head * H + d0 + k));
+    int8_t* dst = reinterpret_cast<int8_t*>(base) + row * H + d0;
+    if constexpr (V == 4) *reinterpret_cast<char4*>(dst) = q4[0];
+    else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
+  } else {
+    store_n<CacheT, V>(reinterpret_cast<CacheT*>(base) + row * H + d0, y);
+  }
+}
+
 // T: element type of query/key/value. CacheT: element type of the cache
-// (T, or int8_t for a quantised cache). QT: element type of prepared queries.
+// (T, int8_t for an int8 cache, uint8_t for a 4-bit cache). QT: element type
+// of prepared queries.
 template <typename T, typename CacheT, typename QT>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 prepass_kernel(const Params p) {
@@ -161,21 +197,7 @@ prepass_kernel(const Params p) {
                 (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
       store_n<QT, V>(dst, y);
     } else {
-      const long long off = (((long long)b * p.Nkv + head) * p.C + pos) * H + d0;
-      if constexpr (sizeof(CacheT) == 1) {
-        const float* sc = role == kKey ? p.k_scale : p.v_scale;
-        const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
-        char4 q4[V / 4];
-        int8_t* qb = reinterpret_cast<int8_t*>(q4);
-#pragma unroll
-        for (int k = 0; k < V; ++k) qb[k] = quant_i8(y[k], channel_scale(sc, nsc, head * H + d0 + k));
-        int8_t* dst = reinterpret_cast<int8_t*>(role == kKey ? p.present_k : p.present_v) + off;
-        if constexpr (V == 4) *reinterpret_cast<char4*>(dst) = q4[0];
-        else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
-      } else {
-        CacheT* dst = reinterpret_cast<CacheT*>(role == kKey ? p.present_k : p.present_v) + off;
-        store_n<CacheT, V>(dst, y);
-      }
+      append_chunk<CacheT, V>(p, role, b, head, pos, d0, y);
     }
   }
 }
@@ -270,21 +292,7 @@ prepass_vec_kernel(const Params p) {
         QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
         store_n<QT, V>(dst, xr);
       } else {
-        const long long off = (((long long)b * p.Nkv + head) * p.C + pos) * H + d0;
-        if constexpr (sizeof(CacheT) == 1) {
-          const float* sc = role == kKey ? p.k_scale : p.v_scale;
-          const int nsc = role == kKey ? p.k_scale_n : p.v_scale_n;
-          char4 q4[V / 4];
-          int8_t* qb = reinterpret_cast<int8_t*>(q4);
-#pragma unroll
-          for (int k = 0; k < V; ++k) qb[k] = quant_i8(xr[k], channel_scale(sc, nsc, head * H + d0 + k));
-          int8_t* dst = reinterpret_cast<int8_t*>(role == kKey ? p.present_k : p.present_v) + off;
-          if constexpr (V == 4) *reinterpret_cast<char4*>(dst) = q4[0];
-          else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
-        } else {
-          CacheT* dst = reinterpret_cast<CacheT*>(role == kKey ? p.present_k : p.present_v) + off;
-          store_n<CacheT, V>(dst, xr);
-        }
+        append_chunk<CacheT, V>(p, role, b, head, pos, d0, xr);
       }
     }
   }
@@ -349,6 +357,8 @@ cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
                               : launch_vec<__half, __half, float>(p, st, &done);
   else if (p.cache_type == kI8)
     ev = launch_vec<float, int8_t, float>(p, st, &done);
+  else if (p.cache_type == kI4)
+    ev = launch_vec<float, uint8_t, float>(p, st, &done);
   else
     ev = launch_vec<float, float, float>(p, st, &done);
   if (done || ev != cudaSuccess) return ev;
@@ -362,6 +372,8 @@ cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
     else prepass_kernel<__half, __half, float><<<grid, block, 0, st>>>(p);
   } else if (p.cache_type == kI8) {
     prepass_kernel<float, int8_t, float><<<grid, block, 0, st>>>(p);
+  } else if (p.cache_type == kI4) {
+    prepass_kernel<float, uint8_t, float><<<grid, block, 0, st>>>(p);
   } else {
     prepass_kernel<float, float, float><<<grid, block, 0, st>>>(p);
   }
@@ -369,6 +381,7 @@ cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
 }
 
 cudaError_t launch_copy_past(const Params& p, cudaStream_t st) {
+  if (p.cache_type == kI4) return cudaErrorNotSupported;   // a 4-bit cache has no past
   const int esize = p.cache_type == kF32 ? 4 : (p.cache_type == kF16 ? 2 : 1);
   dim3 grid(64, p.B * p.Nkv), block(256);
   copy_past_kernel<<<grid, block, 0, st>>>(p, esize);

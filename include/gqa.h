@@ -87,7 +87,7 @@ typedef struct gqa_attrs {
   int32_t smooth_softmax;       /* -1 (default); 1 adds exp(0 - max) to the denominator when no head_sink */
   int32_t k_quant_type;         /* gqa_quant; NONE (default) */
   int32_t v_quant_type;         /* gqa_quant; NONE (default) */
-  int32_t kv_cache_bit_width;   /* 8 for an int8 cache (4 is UNSUPPORTED); ignored when not quantised */
+  int32_t kv_cache_bit_width;   /* 8: int8 cache; 4: packed 4-bit cache (prompt only); ignored when not quantised */
   int32_t sliding_window_cache; /* 0 (default); 1 is UNSUPPORTED */
 } gqa_attrs;
 
@@ -96,7 +96,7 @@ typedef struct gqa_attrs {
  *   key, value     T      (B, S, N_kv*H)            -- kv_sequence_length == S
  *   past_key/value T_CACHE (B, N_kv, L, H) or absent. L is the capacity when
  *                  past and present are one buffer (past.data == present.data),
- *                  else the past length (copy mode).
+ *                  else the past length (copy mode). Absent for a 4-bit cache.
  *   seqlens_k      int32  (B): total length of batch b minus one (device)
  *   cos/sin_cache  T      (R, H/2), R > largest position; required iff do_rotary
  *   attention_bias T      (B or 1, N or 1, S, total_sequence_length) or absent
@@ -118,7 +118,11 @@ typedef struct gqa_inputs {
 
 /* Outputs, section Outputs: output T (B, S, N*H); present_key/value T_CACHE
  * (B, N_kv, C, H). Shared buffer: present.data == past.data and C == L.
- * Copy mode: C == L + S. No past: C >= S (a capacity buffer). */
+ * Copy mode: C == L + S. No past: C >= S (a capacity buffer).
+ * 4-bit cache (kv_cache_bit_width == 4, section Inputs past_key / present_key):
+ * GQA_U8 of shape (B, N_kv, C, H/2); byte k of a row holds code(2k) + 8 in
+ * its low nibble and code(2k+1) + 8 in its high nibble, code =
+ * clamp(rint(x / scale), -7, 7) with the fp32 division of the int8 code. */
 typedef struct gqa_outputs {
   gqa_tensor output;
   gqa_tensor present_key, present_value;
@@ -133,8 +137,8 @@ GQA_API void gqa_attrs_default(gqa_attrs* attrs);
  * Returns INVALID_ARGUMENT for a NULL pointer, non-positive head counts,
  * num_heads % kv_num_heads != 0, causal == 0 with local_window_size != -1,
  * local_window_size < -1, softcap < 0, a non-finite scale or epsilon, or a
- * quant type outside gqa_quant; UNSUPPORTED for sliding_window_cache == 1 and
- * kv_cache_bit_width == 4 (int4 cache). */
+ * quant type outside gqa_quant, or a quantised cache whose kv_cache_bit_width
+ * is neither 8 nor 4; UNSUPPORTED for sliding_window_cache == 1. */
 GQA_API gqa_status gqa_create(const gqa_attrs* attrs, gqa_handle** out);
 
 /* Bytes of device workspace gqa_forward needs for these shapes (host-only;
@@ -147,7 +151,8 @@ GQA_API gqa_status gqa_workspace_size(const gqa_handle* handle, const gqa_inputs
  *   1. append the S new K/V rows of every (batch, KV head) at positions
  *      past_b .. past_b+S-1 of the present cache, past_b = seqlens_k[b]+1-S
  *      with a past cache and 0 without (K: RMS norm, then rotary at the
- *      absolute position, then cast or int8-quantise; V: cast or quantise);
+ *      absolute position, then cast, int8-quantise or pack 4-bit codes;
+ *      V: the same store without norm or rotary);
  *      in copy mode the live past rows 0 .. past_b-1 are copied first;
  *   2. output[b, i, h] = softmax over the visible cache rows of
  *      scale * q_h . k (softcapped, plus bias), with query head h reading KV

@@ -7,8 +7,8 @@ RMS norm / rotary, whose stored value must be the fp16 rounding of a value
 within the fp32 compute error (8 fp32 ulps of the row's largest value) of the
 oracle's fp64 value (fp16; where rotary cancels a value into the fp16
 subnormal range that error spans more than one fp16 ulp), within 4 fp32 ulps
-of the row scale (fp32), or, for int8 codes, either integer when x/scale
-lies within 1e-3 of a half-integer.
+of the row scale (fp32), or, for int8 and 4-bit codes, either integer when
+x/scale lies within 1e-3 of a half-integer.
 """
 
 from __future__ import annotations
@@ -110,12 +110,14 @@ def _allowed_k_mismatch(case, ref, b, g, pos, gpu_row, ref_row):
         y = gpu_row.astype(np.float64)
         bound = 4 * 2.0 ** -24 * (np.abs(x).max() + np.abs(x))
         return bool(np.all(np.abs(y - x) <= bound))
-    if gpu_row.dtype == np.int8:
+    if gpu_row.dtype in (np.int8, np.uint8):
         qt = case["attrs"]["k_quant_type"]
         H = x.shape[0]
         sc = np.asarray(inp["k_scale"], np.float32).reshape(-1)
         sc = np.full(H, sc[0], np.float32) if qt == "PER_TENSOR" else sc[g * H:(g + 1) * H]
         t = x.astype(np.float32) / sc
+        if gpu_row.dtype == np.uint8:     # packed 4-bit codes: compare the codes
+            gpu_row, ref_row = oracle.unpack_int4(gpu_row), oracle.unpack_int4(ref_row)
         diff = gpu_row.astype(np.int32) - ref_row.astype(np.int32)
         near_tie = np.abs(np.abs(t - np.trunc(t)) - 0.5) < 1e-3
         return bool(np.all((diff == 0) | ((np.abs(diff) == 1) & near_tie)))

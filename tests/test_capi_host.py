@@ -53,7 +53,8 @@ def test_attrs_defaults_match_page():
     (dict(num_heads=4, kv_num_heads=2, softcap=-1.0), capi.GQA_ERR_INVALID_ARGUMENT),
     (dict(num_heads=4, kv_num_heads=2, k_quant_type=7), capi.GQA_ERR_INVALID_ARGUMENT),
     (dict(num_heads=4, kv_num_heads=2, sliding_window_cache=1), capi.GQA_ERR_UNSUPPORTED),
-    (dict(num_heads=4, kv_num_heads=2, k_quant_type=2, v_quant_type=2, kv_cache_bit_width=4), capi.GQA_ERR_UNSUPPORTED),
+    (dict(num_heads=4, kv_num_heads=2, k_quant_type=2, v_quant_type=2, kv_cache_bit_width=5),
+     capi.GQA_ERR_INVALID_ARGUMENT),
 ])
 def test_create_rejects(kw, status):
     with pytest.raises(capi.GqaError) as e:
@@ -67,7 +68,9 @@ class FakeCall:
     def __init__(self, dtype="f16", B=2, S=1, N=8, Nkv=2, H=128, C=64, mode="shared", **feat):
         self.next = 0x10000
         t = capi.GQA_F16 if dtype == "f16" else capi.GQA_F32
-        cache_t = capi.GQA_I8 if feat.get("quant") else t
+        bits = feat.get("bits", 8)
+        cache_t = (capi.GQA_U8 if bits == 4 else capi.GQA_I8) if feat.get("quant") else t
+        row = H // 2 if feat.get("quant") and bits == 4 else H
         self.inp = capi.GqaInputs()
         self.out = capi.GqaOutputs()
         self.inp.query = self.t(t, (B, S, N * H))
@@ -76,8 +79,8 @@ class FakeCall:
         self.inp.seqlens_k = self.t(capi.GQA_I32, (B,))
         self.inp.total_sequence_length = C if mode != "prompt" else S
         self.out.output = self.t(t, (B, S, N * H))
-        self.out.present_key = self.t(cache_t, (B, Nkv, C, H))
-        self.out.present_value = self.t(cache_t, (B, Nkv, C, H))
+        self.out.present_key = self.t(cache_t, (B, Nkv, C, row))
+        self.out.present_value = self.t(cache_t, (B, Nkv, C, row))
         if mode == "shared":
             self.inp.past_key = self.out.present_key
             self.inp.past_value = self.out.present_value
@@ -87,7 +90,7 @@ class FakeCall:
             self.inp.v_scale = self.t(capi.GQA_F32, (n,))
         self.attrs = dict(num_heads=N, kv_num_heads=Nkv)
         if feat.get("quant"):
-            self.attrs.update(k_quant_type=feat["quant"], v_quant_type=feat["quant"])
+            self.attrs.update(k_quant_type=feat["quant"], v_quant_type=feat["quant"], kv_cache_bit_width=bits)
 
     def t(self, dtype, shape):
         self.next += 1 << 24
@@ -179,6 +182,28 @@ def test_optional_input_errors():
     c = FakeCall()
     c.inp.attention_bias = c.t(capi.GQA_F16, (1, 1, 1, 64))               # broadcast dims: fine
     assert c.size() > 0
+
+
+def test_int4_cache_checks():
+    """A 4-bit cache: uint8 rows of H/2 bytes, fp32 Q/K/V, prompt only, always the prefill regime."""
+    c = FakeCall(dtype="f32", S=1, C=8, mode="prompt", quant="PER_CHANNEL", bits=4)
+    assert c.size() > 0
+    h = capi.gqa_create(capi.make_attrs(**c.attrs))
+    try:
+        assert capi.gqa_describe_plan(h, c.inp, c.out).regime == capi.GQA_REGIME_PREFILL
+    finally:
+        capi.gqa_destroy(h)
+    c = FakeCall(dtype="f32", S=1, C=8, mode="shared", quant="PER_TENSOR", bits=4)   # a past cache
+    _expect(c, capi.GQA_ERR_UNSUPPORTED)
+    c = FakeCall(dtype="f32", S=4, C=8, mode="prompt", quant="PER_CHANNEL", bits=4)
+    c.out.present_key = c.t(capi.GQA_U8, (2, 2, 8, 128))                 # row of H bytes, not H/2
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall(dtype="f32", S=4, C=8, mode="prompt", quant="PER_CHANNEL", bits=4)
+    c.out.present_key = c.t(capi.GQA_I8, (2, 2, 8, 64))                  # int8 dtype for a 4-bit cache
+    c.out.present_value = c.t(capi.GQA_I8, (2, 2, 8, 64))
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall(dtype="f32", S=4, C=8, mode="prompt", quant="PER_CHANNEL")
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, kv_cache_bit_width=4)     # int8 buffers, 4-bit attribute
 
 
 def test_total_length_beyond_capacity_rejected():

@@ -86,6 +86,21 @@ PREFILL = {
                                  seqlens_k=(129, 100, 7), seqlens_range=None),
     "f16_tc_smooth_multi_block": spec(B=2, S=300, N=8, Nkv=2, capacity=2500, seqlens_range=(300, 2400),
                                       smooth_softmax=1, rotary_theta=1e4),
+    # 4-bit prompt cache (fp32 Q/K/V): packed nibbles written by the pre-pass, unpacked by the prefill
+    "i4_per_channel_prompt_padding": spec(dtype="f32", S=37, N=8, Nkv=2, mode="prompt", capacity=40,
+                                          seqlens_k=(36, 20, 0), seqlens_range=None, quant="PER_CHANNEL", bits=4,
+                                          scale_range=(0.15, 0.4)),
+    "i4_per_tensor_h64_norm_rotary": spec(dtype="f32", H=64, N=8, Nkv=2, S=50, mode="prompt", capacity=64,
+                                          seqlens_k=(49, 49, 30), seqlens_range=None, quant="PER_TENSOR", bits=4,
+                                          qk_norm=True, rotary_theta=1e4, scale_range=(0.2, 0.3)),
+    "i4_s1_prompt": spec(dtype="f32", S=1, mode="prompt", capacity=2, seqlens_k=(0, 0, 0), seqlens_range=None,
+                         quant="PER_CHANNEL", bits=4),
+    "i4_bidirectional_softcap_sink": spec(dtype="f32", N=4, Nkv=2, S=33, mode="prompt", capacity=33, causal=0,
+                                          seqlens_k=(32, 20, 5), seqlens_range=None, quant="PER_TENSOR", bits=4,
+                                          softcap=20.0, head_sink=True, scale_range=(0.2, 0.3)),
+    "i4_h256_window_generic_prepass": spec(dtype="f32", H=256, N=4, Nkv=2, S=20, mode="prompt", capacity=24,
+                                           seqlens_k=(19, 19, 10), seqlens_range=None, quant="PER_CHANNEL", bits=4,
+                                           local_window_size=5, scale_range=(0.1, 0.3)),
 }
 
 
