@@ -37,6 +37,8 @@ from grouped_query_attention_gb300.inputs import WORKLOADS, generate  # noqa: E4
 METRIC = "decode KV-cache GB/s & prefill TFLOP/s, as fraction of GB300 roofline"
 DEFAULT_WORKLOAD = "decode_f16_b16_c8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 CUDA-core peak: 152 SMs x 128 fp32 FMA lanes x 2 flop per clock at the maximum SM clock.
+FP32_LANES_PER_SM, SM_COUNT = 128, 152
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -67,8 +69,8 @@ def visible_pairs(case) -> tuple[int, int]:
 def work(case) -> dict:
     sp = case["spec"]
     pairs, kv_rows = visible_pairs(case)
-    esize = 1 if sp.quant != "NONE" else (2 if sp.dtype == "f16" else 4)
-    kv_bytes = kv_rows * sp.H * 2 * esize
+    esize = (0.5 if sp.bits == 4 else 1) if sp.quant != "NONE" else (2 if sp.dtype == "f16" else 4)
+    kv_bytes = int(kv_rows * sp.H * 2 * esize)
     flops = 4.0 * sp.H * pairs
     decode = sp.S * (sp.N // sp.Nkv) <= 8
     if decode:
@@ -359,10 +361,19 @@ def run_gpu_arm(args, world, rank, local) -> None:
                   "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
                   "copy_past": ["prepass.cu"]}[dominant]
+    peak_key = "hbm_gbs" if wk["bound"] == "hbm" else "bf16_tflops"
     if wk["bound"] == "hbm":
         achieved = wk["kv_bytes"] / (dom_ms / 1e3) / 1e9
         peak = float(peaks["hbm_gbs"])
         unit = "GB/s"
+    elif dominant == "prefill_cuda_core":
+        # fp32 attention on the CUDA cores: bound by fp32 FMA issue, not by the tensor pipe.
+        wk["bound"] = "alu"
+        achieved = wk["flops"] / (dom_ms / 1e3) / 1e12
+        sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        peak = round(SM_COUNT * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12, 2)
+        peak_key = f"fp32 FMA: {SM_COUNT} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x {sm_mhz:.0f} MHz"
+        unit = "TFLOP/s"
     else:
         achieved = wk["flops"] / (dom_ms / 1e3) / 1e12
         peak = float(peaks["bf16_tflops"])
@@ -392,14 +403,15 @@ def run_gpu_arm(args, world, rank, local) -> None:
         "data": "synthetic (seeded numpy, shapes and distributions of the workload)",
         "config": {"workload": args.workload, "batch": sp.B, "seq_len": sp.S, "num_heads": sp.N,
                    "kv_num_heads": sp.Nkv, "head_size": sp.H, "capacity": sp.capacity,
-                   "cache": sp.quant if sp.quant != "NONE" else sp.dtype,
+                   "cache": (f"{sp.quant} int{sp.bits}" if sp.quant != "NONE" else sp.dtype),
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then read back)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "regime": "decode" if plan.regime == 1 else "prefill",
                    "split_len": int(plan.split_len), "max_splits": int(plan.max_splits)},
         "roofline": {"bound": wk["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peaks_src} ({'hbm_gbs' if wk['bound'] == 'hbm' else 'bf16_tflops'}, burst)",
+                     "peak_source": (f"derived ({peak_key})" if wk["bound"] == "alu"
+                                     else f"{peaks_src} ({peak_key}, burst)"),
                      "kernel": dominant, "kernel_ms": round(dom_ms, 5)},
         "kernels_ms": {k: round(sum(v) / len(v), 5) for k, v in per_kernel.items()},
         "e2e": {"value": round(e2e_value, 3), "unit": wk["unit"], "h2d_bytes_per_step": int(h2d),

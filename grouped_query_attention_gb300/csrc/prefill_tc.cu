@@ -13,6 +13,11 @@
 //                live-length masks, softcap, bias, online max with lazy
 //                rescaling of O in tensor memory, P written back over S as
 //                fp16, epilogue O / l (+ sink term) to the output.
+//                With a bias shared by all heads (G >= 8) warp 0 also stages
+//                the bias block of each key tile (the CTA's distinct query
+//                positions x 128 keys, fp32 times log2(e)) into a 2-stage
+//                shared-memory ring with coalesced loads, so the softmax
+//                threads read it with 16-byte shared loads.
 // The two softmax groups ping-pong: while one works on its tile the tensor
 // core runs the other's MMAs. Tensor memory: S0 | S1 | O0 | O1 (512 columns).
 // Every barrier wait is bounded; on expiry the CTA sets the TIMEOUT status
@@ -38,7 +43,12 @@ constexpr int kBM = 128;                        // rows per query tile
 constexpr int kBN = 128;                        // keys per K/V tile
 constexpr int kHD = 128;                        // head size
 constexpr int kNS = 2;                          // K/V stages
-constexpr int kThreads = 320;                   // 10 warps
+constexpr int kBiasRows = 33;                   // staged bias rows (distinct query positions of a CTA, G >= 8)
+
+// Kernel variants: scores without softcap and bias; softcap and/or bias read
+// by each softmax thread; bias staged in shared memory by a loader warp.
+enum PrefillMode { kPlain = 0, kGeneric = 1, kStagedBias = 2 };
+__host__ __device__ constexpr int threads_for(int) { return 320; }
 constexpr uint32_t kBox = 128u * 128u;          // one 64-column box of 128 rows (fp16) = 16 KB
 constexpr uint32_t kTile = 2u * kBox;           // 128 rows x 128 columns = 32 KB
 constexpr float kLazy = 8.0f;                   // log2 growth tolerated before rescaling O
@@ -49,13 +59,16 @@ struct __align__(1024) TcSmem {
   uint8_t q[2][kTile];
   uint8_t k[kNS][kTile];
   uint8_t v[kNS][kTile];
+  float bias[kNS][kBiasRows][kBN];                // staged bias rows, fp32 times log2(e)
   uint64_t q_full;
   uint64_t k_full[kNS], v_full[kNS], kv_empty[kNS];
+  uint64_t bias_full[kNS], bias_empty[kNS];
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem;
   int abort;
 };
+static_assert(sizeof(TcSmem) + 1024 <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                            bool accumulate) {
@@ -72,18 +85,59 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// c * tanh(x / c) through exp2: tanh(u) = 1 - 2 / (exp(2u) + 1).
-__device__ __forceinline__ float softcap_apply(float x, float c, float inv_c) {
-  const float e = ex2(2.0f * kLog2e * x * inv_c);
-  return c * (1.0f - 2.0f * rcp_approx(e + 1.0f));
+// Constants of the transformed score in the log2 domain.
+//   no softcap: x = raw * scale * log2(e) + bias * log2(e)
+//   softcap c:  c * tanh(raw * scale / c) * log2(e) + bias * log2(e), with
+//               tanh(u) = 1 - 2 / (exp(2u) + 1): e2 = exp2(raw * k_exp),
+//               x = c log2(e) - 2 c log2(e) / (e2 + 1).
+//   softcap, |u| = |raw * scale / c| <= 1/2 (every lane of a warp): the
+//               same value on the FMA pipe, c tanh(u) log2(e) =
+//               raw * scale * log2(e) * P(u^2), P below.
+struct ScoreConst {
+  float k_raw;    // raw multiplier: scale * log2(e) (no softcap) or 2 * scale * log2(e) / c
+  float k_mul;    // -2 c log2(e)
+  float k_add;    // c log2(e)
+  float k_u;      // scale / c
+  float k_w;      // scale * log2(e)
+  float raw_poly; // largest |raw| with |u| <= 1/2
+};
+
+__device__ __forceinline__ ScoreConst score_const(const Params& p) {
+  ScoreConst k;
+  k.k_raw = p.softcap > 0.f ? 2.0f * kLog2e * p.scale / p.softcap : p.scale * kLog2e;
+  k.k_mul = -2.0f * p.softcap * kLog2e;
+  k.k_add = p.softcap * kLog2e;
+  k.k_u = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
+  k.k_w = p.scale * kLog2e;
+  k.raw_poly = 0.5f / fabsf(k.k_u);
+  return k;
 }
 
-// Transformed score in the log2 domain: scale, softcap, + bias.
-__device__ __forceinline__ float score(float raw, float bias, float qk_scale, float cap, float inv_cap) {
-  float x = raw * qk_scale;
-  if (cap > 0.f) x = softcap_apply(x, cap, inv_cap) * kLog2e;
-  return x + bias * kLog2e;
+// tanh(u) / u = P(u^2) for |u| <= 1/2: degree-5 least-squares fit in z = u^2
+// over [0, 1/4] (Chebyshev nodes, weighted for relative error), coefficients
+// rounded to fp32: relative error 3.5e-9 in exact arithmetic, about 1.2 fp32
+// ulps when evaluated by Horner's rule in fp32.
+constexpr float kTanhP1 = -3.333332539e-01f;
+constexpr float kTanhP2 = 1.333289742e-01f;
+constexpr float kTanhP3 = -5.389288813e-02f;
+constexpr float kTanhP4 = 2.127229236e-02f;
+constexpr float kTanhP5 = -6.609579083e-03f;
+
+// Softcapped score of two raw products on the FMA pipe (|u| <= 1/2), log2 domain.
+__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k) {
+  const float2 zero = make_float2(0.f, 0.f);
+  const float2 u = ffma2(raw, make_float2(k.k_u, k.k_u), zero);
+  const float2 z = ffma2(u, u, zero);
+  float2 q = ffma2(z, make_float2(kTanhP5, kTanhP5), make_float2(kTanhP4, kTanhP4));
+  q = ffma2(q, z, make_float2(kTanhP3, kTanhP3));
+  q = ffma2(q, z, make_float2(kTanhP2, kTanhP2));
+  q = ffma2(q, z, make_float2(kTanhP1, kTanhP1));
+  q = ffma2(q, z, make_float2(1.f, 1.f));
+  const float2 w = ffma2(raw, make_float2(k.k_w, k.k_w), zero);
+  return ffma2(w, q, zero);
 }
+
+
 
 // Bias values of keys j .. j+31 (columns col0 .. col0+31 of the tile); zeros
 // without a bias. 16-byte loads only where the address is 16-byte aligned and
@@ -124,11 +178,17 @@ __device__ __forceinline__ void set_abort(const Params& p, TcSmem& sm) {
   flag_status(p, GQA_DEVICE_TIMEOUT_BIT);
 }
 
-// PLAIN: no softcap and no bias (the scores are the scaled products).
-template <bool PLAIN>
-__global__ void __launch_bounds__(kThreads, 1)
+// MODE (PrefillMode): kPlain has no softcap and no bias (the scores are the
+// scaled products); kGeneric reads the bias per thread; kStagedBias adds the
+// bias loader warp. CAP: softcap > 0 (compile-time, so that the 32 scores of
+// a group are independent straight-line chains the scheduler can interleave).
+template <int MODE, bool CAP>
+__global__ void __launch_bounds__(threads_for(MODE), 1)
 prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
+  constexpr bool PLAIN = MODE == kPlain;
+  constexpr bool STAGED = MODE == kStagedBias;
+  constexpr int kThreads = threads_for(MODE);
   extern __shared__ uint8_t smem_raw[];
   TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -178,6 +238,12 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       mbar_init(&sm.p_full[q], kBM);
       mbar_init(&sm.o_done[q], 1);
     }
+    if constexpr (STAGED) {
+      for (int s = 0; s < kNS; ++s) {
+        mbar_init(&sm.bias_full[s], 32);          // every loader lane
+        mbar_init(&sm.bias_empty[s], 8);          // one lane of every softmax warp
+      }
+    }
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     mbar_fence_init();
@@ -191,7 +257,21 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    // The whole warp waits; one elected lane issues.
+    // The whole warp waits; one elected lane issues. With a staged bias the
+    // warp then loads the bias block of the same key tile: stage s holds
+    // bias[bb, 0, i_lo + rho, j0 .. j0+127] * log2(e) in fp32 for the CTA's
+    // positions rho = 0 .. nbr-1, and -inf where key j0+col is not visible
+    // from position past + i_lo + rho (beyond the live length, causal bound,
+    // window floor): the visibility mask of every head at that position, so
+    // the softmax threads add it and need no mask of their own. Lane l moves
+    // the key pairs (2l, 2l+1) and (64+2l, 65+2l) of each row; the loads of
+    // 17 rows are issued before any of them is stored.
+    const int nbr = STAGED ? min(i_hi - i_lo + 1, kBiasRows) : 0;   // the host checks the span fits
+    const unsigned short* bias0 =
+        STAGED ? reinterpret_cast<const unsigned short*>(p.bias) + ((long long)(p.bias_bdim > 1 ? b : 0) * p.S + i_lo) * p.bias_ld
+               : nullptr;
+    const int T = p.bias_ld;
+    constexpr int kRowsPerBatch = 17;
     if (elect_one()) {
       mbar_arrive_tx(&sm.q_full, 2 * kTile);
       for (int q = 0; q < 2; ++q)
@@ -215,6 +295,53 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       }
       __syncwarp();
       issued = t + 1;
+      if constexpr (STAGED) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.bias_empty[st], ph ^ 1u)) || aborted(sm)) {
+          if (lane == 0) set_abort(p, sm);
+          break;
+        }
+        const int j0 = kmin + t * kBN;
+        const int ja = j0 + 2 * lane, jb = j0 + 64 + 2 * lane;
+        // Unconditional loads at clamped (in-bounds) positions, selected after:
+        // no branch separates the loads, so all of a batch are in flight at once.
+        const int ka0 = min(ja, T - 1), ka1 = min(ja + 1, T - 1), kb0 = min(jb, T - 1), kb1 = min(jb + 1, T - 1);
+        const uint32_t ma0 = ja < T ? 0xffffu : 0u, ma1 = ja + 1 < T ? 0xffffu : 0u;
+        const uint32_t mb0 = jb < T ? 0xffffu : 0u, mb1 = jb + 1 < T ? 0xffffu : 0u;
+        for (int base = 0; base < nbr; base += kRowsPerBatch) {
+          uint32_t a[kRowsPerBatch], c[kRowsPerBatch];   // two fp16 bit patterns each, low = even key
+#pragma unroll
+          for (int k = 0; k < kRowsPerBatch; ++k) {
+            const unsigned short* src = bias0 + (long long)min(base + k, nbr - 1) * T;
+            a[k] = ((uint32_t)__ldg(src + ka0) & ma0) | (((uint32_t)__ldg(src + ka1) & ma1) << 16);
+            c[k] = ((uint32_t)__ldg(src + kb0) & mb0) | (((uint32_t)__ldg(src + kb1) & mb1) << 16);
+          }
+#pragma unroll
+          for (int k = 0; k < kRowsPerBatch; ++k) {
+            if (base + k >= nbr) break;
+            const int pos = past + i_lo + base + k;
+            const int vlo = p.window >= 0 ? pos - p.window : 0;              // first visible key
+            const int vhi = p.causal ? min(total, pos + 1) : total;          // one past the last
+            float2* dst = reinterpret_cast<float2*>(&sm.bias[st][base + k][0]);
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a[k]));
+            const float2 fc = __half22float2(*reinterpret_cast<const __half2*>(&c[k]));
+            dst[lane] = make_float2(ja >= vlo && ja < vhi ? fa.x * kLog2e : -INFINITY,
+                                    ja + 1 >= vlo && ja + 1 < vhi ? fa.y * kLog2e : -INFINITY);
+            dst[32 + lane] = make_float2(jb >= vlo && jb < vhi ? fc.x * kLog2e : -INFINITY,
+                                         jb + 1 >= vlo && jb + 1 < vhi ? fc.y * kLog2e : -INFINITY);
+          }
+        }
+        mbar_arrive(&sm.bias_full[st]);
+        // Pull the next tile's bias lines into L1 so that its loads are short:
+        // 128-byte lines covering keys j0+128 .. j0+255 of every row (addresses
+        // clamped into the row).
+        if (t + 1 < ntiles) {
+          for (int x = lane; x < nbr * 3; x += 32) {
+            const int rho = x / 3, ln = x - rho * 3;
+            const int col = min(j0 + kBN + ln * 64, T - 1);
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(bias0 + (long long)rho * T + col));
+          }
+        }
+      }
     }
     // Drain: no copy of this CTA may still be landing when it exits.
     mbar_wait(&sm.q_full, 0);
@@ -226,17 +353,17 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     // ================================================================ MMA issuer
     // Shared-memory descriptors built once; a K step adds its start-address
     // offset (16-byte units). One elected lane issues, the warp stays converged.
-    uint64_t dq[2], dk[kNS], dv[kNS];
+    // Stage s of the K (V) ring starts kTile bytes after stage s-1: its
+    // descriptor is the stage-0 one plus that offset in 16-byte units (the
+    // start-address field cannot overflow: shared addresses are below 256 KB).
+    uint64_t dq[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) dq[i] = desc_kmajor_sw128(smem_addr(sm.q[i]));
-#pragma unroll
-    for (int i = 0; i < kNS; ++i) {
-      dk[i] = desc_kmajor_sw128(smem_addr(sm.k[i]));
-      dv[i] = desc_mnmajor_sw128(smem_addr(sm.v[i]), kBox, 1024);
-    }
+    const uint64_t dk0 = desc_kmajor_sw128(smem_addr(sm.k[0]));
+    const uint64_t dv0 = desc_mnmajor_sw128(smem_addr(sm.v[0]), kBox, 1024);
     auto issue_s = [&](int q, int st) {
       const uint32_t d = tmem + q * 128;
-      const uint64_t a0 = dq[q], b0 = dk[st];
+      const uint64_t a0 = dq[q], b0 = dk0 + (uint64_t)(st * (int)(kTile >> 4));
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint64_t off = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
@@ -247,7 +374,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     auto issue_pv = [&](int q, int st, bool acc) {
       const uint32_t d = tmem + 256 + q * 128;
       const uint32_t pa = tmem + q * 128;  // P over the first 64 columns of S_q
-      const uint64_t b0 = dv[st];
+      const uint64_t b0 = dv0 + (uint64_t)(st * (int)(kTile >> 4));
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) mma_f16_ts(d, pa + ks * 8, b0 + (uint64_t)(ks * 128), kIdO, acc || ks > 0);
       mma_commit(&sm.o_done[q]);
@@ -333,16 +460,18 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     const uint32_t s_addr = tmem + lane_addr + q * 128;
     const uint32_t o_addr = tmem + lane_addr + 256 + q * 128;
     const float qk_scale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
-    const float inv_cap = p.softcap > 0.f ? 1.0f / p.softcap : 0.f;
     const __half* bias_row = nullptr;
-    if (p.has_bias && live)
+    if (!STAGED && p.has_bias && live)
       bias_row = reinterpret_cast<const __half*>(p.bias) +
                  (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
                      p.bias_ld;
+    const int brow = live ? i - i_lo : 0;     // staged bias row of this thread (any in-range row when not live)
+    const ScoreConst kc = score_const(p);
     float m_run = kNegBig, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      const bool got = mbar_wait(&sm.s_full[q], (uint32_t)t & 1u) && !aborted(sm);
+      bool got = mbar_wait(&sm.s_full[q], (uint32_t)t & 1u) && !aborted(sm);
+      if constexpr (STAGED) got = got && mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u);
       if (!__all_sync(0xffffffffu, got)) {   // the warp leaves together
         ok = false;
         break;
@@ -352,106 +481,203 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       const int lo = max(lo_key - j0, 0), hi = min(hi_key - j0, kBN);   // visible columns [lo, hi)
       // Warp-uniform fast path: no row of this warp needs a mask on this tile.
       const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kBN);
-      // Pass 1: row max in the log2 domain. Plain scores: the whole row with
-      // four loads in flight and one wait, max of the raw products scaled once
-      // (the scale is positive). Softcap / bias: two halves of 64 columns,
-      // transformed in place and written back over S for pass 2.
-      float mt = kNegBig;
+      // Plain scores: pass 1 takes the row max over the whole row (four loads
+      // in flight, one wait, the raw products scaled once: the scale is
+      // positive), pass 2 writes P = exp2(score - m) over S. Softcap / bias:
+      // one pass per half of 64 columns: transform, half max, raise the
+      // reference max when the half exceeds it by more than 2^8 (rescaling O,
+      // l and the half already written), exp2 and pack P.
+      float2 ls2 = make_float2(0.f, 0.f);
       if constexpr (PLAIN) {
-        uint32_t r[kBN];
+        float mt = kNegBig;
+        {
+          uint32_t r[kBN];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, r + c * 32);
-        tmem_ld_wait();
-        float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
-        if (!full) {
-          // Masked columns become -inf in tensor memory too, so pass 2 needs
-          // no mask (the scale is positive: exp2 of -inf * scale - m is 0).
+          for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, r + c * 32);
+          tmem_ld_wait();
+          float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
+          if (!full) {
+            // Masked columns become -inf in tensor memory too, so pass 2 needs
+            // no mask (the scale is positive: exp2 of -inf * scale - m is 0).
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) r[e] = (e >= lo && e < hi) ? r[e] : 0xff800000u;
+            for (int e = 0; e < kBN; ++e) r[e] = (e >= lo && e < hi) ? r[e] : 0xff800000u;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_st32(s_addr + c * 32, r + c * 32);
-          tmem_st_wait();
+            for (int c = 0; c < 4; ++c) tmem_st32(s_addr + c * 32, r + c * 32);
+            tmem_st_wait();
+          }
+#pragma unroll
+          for (int e = 0; e < kBN; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+          const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          mt = m > kNegBig ? m * qk_scale : kNegBig;
         }
+        // Lazy rescale: a row moves its reference max only when the tile max
+        // exceeds it by more than 2^8. The tensor-memory traffic is warp-wide,
+        // so the whole warp takes the branch and lanes that keep their max use f = 1.
+        const bool grow = mt > m_run + kLazy;
+        const float m_new = grow ? mt : m_run;
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_q is complete up to tile t-1 (its MMAs precede S_q(t)): rescale it in place.
+          const float f = grow ? ex2(m_run - m_new) : 1.0f;
 #pragma unroll
-        for (int e = 0; e < kBN; e += 2)
-          m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-        const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        mt = m > kNegBig ? m * qk_scale : kNegBig;
-      } else {
+          for (int c = 0; c < 4; ++c) {
+            uint32_t raw[32];
+            tmem_ld32(o_addr + c * 32, raw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+            tmem_st32(o_addr + c * 32, raw);
+          }
+          l_run *= f;
+        }
+        m_run = m_new;
+        // Pass 2: P = exp2(score - m) as fp16 pairs over the first 64 columns of
+        // S_q, 64 scores per load batch; columns are overwritten only after read.
+        const float neg_m = -m_run;
+        const float2 scale2 = make_float2(qk_scale, qk_scale), negm2 = make_float2(neg_m, neg_m);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[64];
           tmem_ld32(s_addr + hf * 64, r);
           tmem_ld32(s_addr + hf * 64 + 32, r + 32);
           tmem_ld_wait();
+          uint32_t packed[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float xa = __uint_as_float(r[2 * k]), xb = __uint_as_float(r[2 * k + 1]);
+            const float2 arg = ffma2(make_float2(xa, xb), scale2, negm2);
+            const float pa = ex2(arg.x), pb = ex2(arg.y);
+            ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
+            const __half2 hp = __floats2half2_rn(pa, pb);
+            packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
+          }
+          tmem_st32(s_addr + hf * 32, packed);
+        }
+      } else {
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[64];
+          tmem_ld32(s_addr + hf * 64, r);
+          tmem_ld32(s_addr + hf * 64 + 32, r + 32);
+          tmem_ld_wait();
+          bool poly = false;   // softcap on the FMA pipe for this half (warp-uniform)
+          if constexpr (CAP) {
+            float am[4] = {0.f, 0.f, 0.f, 0.f};   // four independent chains
+#pragma unroll
+            for (int e = 0; e < 64; e += 2)
+              am[(e >> 1) & 3] = fmax3(am[(e >> 1) & 3], fabsf(__uint_as_float(r[e])), fabsf(__uint_as_float(r[e + 1])));
+            poly = __all_sync(0xffffffffu, fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])) <= kc.raw_poly);
+          }
 #pragma unroll
           for (int c = 0; c < 64; c += 32) {
             float bv[32];
-            load_bias32(bias_row, j0 + hf * 64 + c, hf * 64 + c, lo, hi, bv);
+            if constexpr (!STAGED) load_bias32(bias_row, j0 + hf * 64 + c, hf * 64 + c, lo, hi, bv);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int col = hf * 64 + c + e;
-              const float x = score(__uint_as_float(r[c + e]), bv[e], qk_scale, p.softcap, inv_cap);
-              const float y = (full || (col >= lo && col < hi)) ? x : -INFINITY;
-              mt = fmaxf(mt, y);
-              r[c + e] = __float_as_uint(y);
+            for (int c16 = 0; c16 < 32; c16 += 16) {   // 16 independent chains at a time
+              float x[16];
+              if (CAP && poly) {
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                  const float2 y = softcap_poly2(
+                      make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1])), kc);
+                  x[e] = y.x;
+                  x[e + 1] = y.y;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[c + c16 + e]) * kc.k_raw;
+                if constexpr (CAP) {
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) x[e] = fmaf(rcp_approx(ex2(x[e]) + 1.0f), kc.k_mul, kc.k_add);
+                }
+              }
+              if constexpr (STAGED) {
+                // Staged bias: fp32, already times log2(e), -inf on masked keys.
+                const float4* b4 = reinterpret_cast<const float4*>(&sm.bias[t % kNS][brow][hf * 64 + c + c16]);
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                  const float4 bq = b4[e4];
+                  x[4 * e4] += bq.x;
+                  x[4 * e4 + 1] += bq.y;
+                  x[4 * e4 + 2] += bq.z;
+                  x[4 * e4 + 3] += bq.w;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = fmaf(bv[c16 + e], kLog2e, x[e]);
+              }
+#pragma unroll
+              for (int e = 0; e < 16; ++e) r[c + c16 + e] = __float_as_uint(x[e]);
             }
           }
-          tmem_st32(s_addr + hf * 64, r);
-          tmem_st32(s_addr + hf * 64 + 32, r + 32);
-        }
-        tmem_st_wait();
-      }
-      // Lazy rescale: a row moves its reference max only when the tile max
-      // exceeds it by more than 2^8. The tensor-memory traffic is warp-wide,
-      // so the whole warp takes the branch and lanes that keep their max use f = 1.
-      const bool grow = mt > m_run + kLazy;
-      const float m_new = grow ? mt : m_run;
-      if (t > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_q is complete up to tile t-1 (its MMAs precede S_q(t)): rescale it in place.
-        const float f = grow ? ex2(m_run - m_new) : 1.0f;
+          if (!STAGED && !full) {   // warp-uniform: only tiles on a mask boundary pay for the selects
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t raw[32];
-          tmem_ld32(o_addr + c * 32, raw);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
-          tmem_st32(o_addr + c * 32, raw);
-        }
-        l_run *= f;
-      }
-      m_run = m_new;
-      // Pass 2: P = exp2(score - m) as fp16 pairs over the first 64 columns of
-      // S_q, 64 scores per load batch; columns are overwritten only after read.
-      const float neg_m = -m_run;
-      const float2 scale2 = make_float2(qk_scale, qk_scale), negm2 = make_float2(neg_m, neg_m);
-      float2 ls2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t r[64];
-        tmem_ld32(s_addr + hf * 64, r);
-        tmem_ld32(s_addr + hf * 64 + 32, r + 32);
-        tmem_ld_wait();
-        uint32_t packed[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float xa = __uint_as_float(r[2 * k]), xb = __uint_as_float(r[2 * k + 1]);
-          float pa, pb;
-          if constexpr (PLAIN) {
-            const float2 arg = ffma2(make_float2(xa, xb), scale2, negm2);
-            pa = ex2(arg.x);
-            pb = ex2(arg.y);
-          } else {   // masked scores are -inf: exp2 gives 0
-            const float2 arg = ffma2(make_float2(xa, xb), make_float2(1.f, 1.f), negm2);
-            pa = ex2(arg.x);
-            pb = ex2(arg.y);
+            for (int e = 0; e < 64; ++e) {
+              const int col = hf * 64 + e;
+              r[e] = (col >= lo && col < hi) ? r[e] : 0xff800000u;   // -inf
+            }
           }
-          ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
-          const __half2 hp = __floats2half2_rn(pa, pb);
-          packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
+          float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+          const float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          const bool grow = mh > m_run + kLazy;
+          if (__any_sync(0xffffffffu, grow)) {   // warp-wide tensor-memory traffic
+            const float m_new = grow ? mh : m_run;
+            const float f = grow ? ex2(m_run - m_new) : 1.0f;
+            if (t > 0) {
+              // O_q is complete up to tile t-1 (its MMAs precede S_q(t)): rescale it in place.
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(o_addr + c * 32, raw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+                tmem_st32(o_addr + c * 32, raw);
+              }
+            }
+            if (hf == 1) {
+              // P of the first half was written with the old reference.
+              uint32_t pk[32];
+              tmem_st_wait();
+              tmem_ld32(s_addr, pk);
+              tmem_ld_wait();
+              const float2 f2 = make_float2(f, f);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
+                const float2 w = ffma2(v, f2, make_float2(0.f, 0.f));
+                const __half2 hw = __floats2half2_rn(w.x, w.y);
+                pk[k] = *reinterpret_cast<const uint32_t*>(&hw);
+              }
+              tmem_st32(s_addr, pk);
+            }
+            l_run *= f;
+            ls2.x *= f;
+            ls2.y *= f;
+            m_run = m_new;
+          }
+          // Masked scores are -inf: exp2 gives 0.
+          const float2 negm2 = make_float2(-m_run, -m_run);
+          uint32_t packed[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float2 arg = ffma2(make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])),
+                                     make_float2(1.f, 1.f), negm2);
+            const float pa = ex2(arg.x), pb = ex2(arg.y);
+            ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
+            const __half2 hp = __floats2half2_rn(pa, pb);
+            packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
+          }
+          tmem_st32(s_addr + hf * 32, packed);
         }
-        tmem_st32(s_addr + hf * 32, packed);
+        if constexpr (STAGED) {
+          // The warp's bias reads have returned (their values are used above).
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.bias_empty[t % kNS]);
+        }
       }
       const float ls = ls2.x + ls2.y;
       l_run += ls;
@@ -518,25 +744,33 @@ cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps) {
 namespace {
 // Dynamic shared memory opt-in, set once per device and kernel variant.
 constexpr int kMaxDevices = 64;
-bool g_smem_set[2][kMaxDevices];
+bool g_smem_set[5][kMaxDevices];
 }  // namespace
 
 cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& maps) {
   const int smem = (int)sizeof(TcSmem) + 1024;
   // The plain kernel scales the row max once, which needs a positive scale.
+  // A bias shared by all heads is staged when a CTA's 256 rows span at most
+  // kBiasRows query positions (255 / G + 2 bounds the span).
   const bool plain = p.softcap <= 0.f && !p.has_bias && p.scale > 0.f;
-  auto kern = plain ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  const bool staged = p.has_bias && p.bias_ndim == 1 && 255 / p.G + 2 <= kBiasRows;
+  const int mode = plain ? kPlain : staged ? kStagedBias : kGeneric;
+  const bool cap = p.softcap > 0.f;
+  auto kern = mode == kPlain ? prefill_tc_kernel<kPlain, false>
+              : mode == kStagedBias ? (cap ? prefill_tc_kernel<kStagedBias, true> : prefill_tc_kernel<kStagedBias, false>)
+                                    : (cap ? prefill_tc_kernel<kGeneric, true> : prefill_tc_kernel<kGeneric, false>);
+  const int variant = mode == kPlain ? 0 : 1 + 2 * (mode == kStagedBias) + cap;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_smem_set[plain][dev]) {
+  if (!g_smem_set[variant][dev]) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
-    g_smem_set[plain][dev] = true;
+    g_smem_set[variant][dev] = true;
   }
   const int nrows = p.S * p.G;
   dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
-  kern<<<grid, kThreads, smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2]);
+  kern<<<grid, threads_for(mode), smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2]);
   return cudaGetLastError();
 }
 

@@ -170,10 +170,12 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
                 share_buffer=share, spec=spec)
 
 
-# The five synthetic workloads (sizes and distributions of the operator's use
+# The synthetic workloads (sizes and distributions of the operator's use
 # cases): a tiny fp32 prompt, fp16 decode over a shared cache, fp16 causal
 # prefill with Q/K RMS norm and rotary, fp16 chunked prefill with window,
-# softcap, head sink, bias and rotary, and fp32 decode over an int8 cache.
+# softcap, head sink, bias and rotary, fp32 decode over an int8 cache, and
+# fp32 prompts that build an int8 or a 4-bit cache (the quantised-cache
+# prefill variants of section Implementation variants).
 WORKLOADS = {
     "prompt_f32_b1_s16": CaseSpec(
         name="prompt_f32_b1_s16", dtype="f32", B=1, S=16, N=4, Nkv=2, H=32, capacity=16,
@@ -192,5 +194,11 @@ WORKLOADS = {
     "decode_int8_f32_b32_c16384": CaseSpec(
         name="decode_int8_f32_b32_c16384", dtype="f32", B=32, S=1, N=32, Nkv=8, H=128,
         capacity=16384, mode="shared", seqlens_range=(4096, 16383), quant="PER_CHANNEL"),
+    "prefill_int8_f32_b2_s2048": CaseSpec(
+        name="prefill_int8_f32_b2_s2048", dtype="f32", B=2, S=2048, N=32, Nkv=8, H=128, capacity=2048,
+        mode="prompt", seqlens_k=(2047, 2047), quant="PER_CHANNEL"),
+    "prefill_int4_f32_b2_s2048": CaseSpec(
+        name="prefill_int4_f32_b2_s2048", dtype="f32", B=2, S=2048, N=32, Nkv=8, H=128, capacity=2048,
+        mode="prompt", seqlens_k=(2047, 2047), quant="PER_TENSOR", bits=4, scale_range=(0.3, 0.5)),
 }
 WORKLOAD_ORDER = list(WORKLOADS)

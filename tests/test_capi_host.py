@@ -120,7 +120,7 @@ def test_valid_calls_have_a_workspace():
 def test_workloads_validate():
     for name, sp in WORKLOADS.items():
         c = FakeCall(dtype=sp.dtype, B=sp.B, S=sp.S, N=sp.N, Nkv=sp.Nkv, H=sp.H, C=sp.capacity,
-                     mode=sp.mode, quant=sp.quant if sp.quant != "NONE" else None)
+                     mode=sp.mode, quant=sp.quant if sp.quant != "NONE" else None, bits=sp.bits)
         assert c.size() > 0, name
 
 

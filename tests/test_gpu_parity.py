@@ -86,6 +86,22 @@ PREFILL = {
                                  seqlens_k=(129, 100, 7), seqlens_range=None),
     "f16_tc_smooth_multi_block": spec(B=2, S=300, N=8, Nkv=2, capacity=2500, seqlens_range=(300, 2400),
                                       smooth_softmax=1, rotary_theta=1e4),
+    # bias shared by all heads with G >= 8: staged through shared memory by the TMA warp
+    "f16_tc_staged_bias_softcap_window": spec(S=70, N=16, Nkv=2, local_window_size=90, softcap=30.0,
+                                              bias=(3, 1, 0.5), head_sink=True, rotary_theta=1e4,
+                                              seqlens_range=(70, 700)),
+    "f16_tc_bias_g6_prompt_padding": spec(S=150, N=12, Nkv=2, mode="prompt", capacity=160,
+                                          seqlens_k=(149, 70, 3), seqlens_range=None, bias=(1, 1, 1.0)),
+    "f16_tc_staged_bias_g8_prompt_padding": spec(S=150, N=16, Nkv=2, mode="prompt", capacity=160,
+                                                 seqlens_k=(149, 70, 3), seqlens_range=None, bias=(1, 1, 1.0)),
+    # bias of large spread: the reference max rises inside a tile (second half) and across tiles
+    "f16_tc_staged_bias_large_spread": spec(S=64, N=16, Nkv=2, softcap=30.0, bias=(1, 1, 8.0),
+                                            seqlens_range=(64, 600)),
+    "f16_tc_per_head_bias_large_spread": spec(S=40, N=4, Nkv=2, bias=(3, 4, 8.0), seqlens_range=(40, 500)),
+    # softcap small against the scores: the exp2 / reciprocal form instead of the polynomial
+    "f16_tc_small_softcap": spec(S=40, N=16, Nkv=2, softcap=1.0, seqlens_range=(40, 700), rotary_theta=1e4),
+    "f16_tc_staged_bias_small_softcap": spec(S=64, N=16, Nkv=2, softcap=2.0, bias=(1, 1, 0.5),
+                                             local_window_size=200, seqlens_range=(64, 600)),
     # 4-bit prompt cache (fp32 Q/K/V): packed nibbles written by the pre-pass, unpacked by the prefill
     "i4_per_channel_prompt_padding": spec(dtype="f32", S=37, N=8, Nkv=2, mode="prompt", capacity=40,
                                           seqlens_k=(36, 20, 0), seqlens_range=None, quant="PER_CHANNEL", bits=4,
