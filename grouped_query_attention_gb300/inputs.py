@@ -63,6 +63,7 @@ class CaseSpec:
     scale: float = 0.0
     quant: str = "NONE"                # NONE | PER_TENSOR | PER_CHANNEL (quantised cache)
     bits: int = 8                      # 8: int8 codes; 4: two 4-bit codes per byte (prompt only)
+    cache_dtype: str | None = None     # float cache dtype of a prompt ("f16" / "f32"); None: the query dtype
     scale_range: tuple = (0.005, 0.02)
     extra: dict = field(default_factory=dict)
 
@@ -107,7 +108,7 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
     B, S, N, Nkv, H = spec.B, spec.S, spec.N, spec.Nkv, spec.H
     quant = spec.quant != "NONE"
     int4 = quant and spec.bits == 4
-    cache_dtype = (np.uint8 if int4 else np.int8) if quant else T
+    cache_dtype = (np.uint8 if int4 else np.int8) if quant else NP_DTYPE[spec.cache_dtype or spec.dtype]
     seqlens = draw_seqlens(spec, seed)
     if seqlens.shape != (B,):
         raise ValueError("seqlens_k must give one value per batch")

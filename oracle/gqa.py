@@ -21,6 +21,10 @@ the readings the library implements):
   * int4 (kv_cache_bit_width = 4) code = clamp(round_half_even(fp32(x) /
     fp32(scale)), -7, 7), stored as the nibble code + 8, two per byte with
     the even coordinate in the low nibble; only prompts (no past cache);
+  * a prompt (no past cache) may store its float cache as float16 or float32
+    whatever the query dtype; attention then reads the new K/V rows as they
+    would be stored in the query dtype (computed from Q/K/V directly, the
+    cache written separately), so the output does not depend on that choice;
   * RMS norm y = x / sqrt(mean(x^2) + eps) * w, weight used as given;
   * padding rows of a prompt (i >= total_b, no past) produce a zero output row;
     their K/V rows are still appended.
@@ -240,6 +244,14 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
     seqlens = np.asarray(inputs["seqlens_k"], dtype=np.int64).reshape(-1)
     total_len = int(np.asarray(inputs["total_sequence_length"]).reshape(-1)[0])
     kq, vq = a["k_quant_type"], a["v_quant_type"]
+    # A prompt's float cache may have another float dtype than the query
+    # (section Description: direct Q/K/V may store its generated cache as
+    # float16 or float32); an existing cache has the query dtype.
+    separate = kq == "NONE" and pk.dtype != out_dtype
+    if separate and (has_past or pk.dtype not in (np.float16, np.float32)):
+        raise ValueError("a float cache of another dtype than the query is only written by a prompt")
+    attn_k = np.zeros((B, Nkv, C, H), dtype=out_dtype) if separate else pk
+    attn_v = np.zeros((B, Nkv, C, H), dtype=out_dtype) if separate else pv
     bits = int(a["kv_cache_bit_width"])
     if kq != "NONE" and bits == 4 and has_past:
         raise ValueError("a 4-bit cache is built by a prompt (no past cache)")
@@ -291,6 +303,9 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 kr = rotary_neox(kr, cos_c[pos], sin_c[pos])
             pk[b, g, pos] = _store(kr, pk.dtype, kq, k_scale, g, H, bits)
             pv[b, g, pos] = _store(vr, pv.dtype, vq, v_scale, g, H, bits)
+            if separate:   # the rows attention reads: the query dtype
+                attn_k[b, g, pos] = kr.astype(out_dtype)
+                attn_v[b, g, pos] = vr.astype(out_dtype)
             new_k[b, g], new_v[b, g] = kr, vr
         new_pos[b] = pos
 
@@ -306,8 +321,8 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 if rows.size == 0:
                     continue
             g = h // G if head_of_group == "block" else h % Nkv
-            kd = _load(pk[b, g, :total_b], kq, k_scale, g, H, bits)
-            vd = _load(pv[b, g, :total_b], vq, v_scale, g, H, bits)
+            kd = _load(attn_k[b, g, :total_b], kq, k_scale, g, H, bits)
+            vd = _load(attn_v[b, g, :total_b], vq, v_scale, g, H, bits)
             qr = q_in[b, rows, h * H:(h + 1) * H].astype(np.float64)
             if qw is not None:
                 qr = rms_norm(qr, qw, eps)

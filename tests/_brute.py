@@ -36,6 +36,10 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
         pv = [[[r.copy() for r in present_value[b, g]] for g in range(Nkv)] for b in range(B)]
         cache_dtype = present_key.dtype
     quant = attrs.get("k_quant_type", "NONE") != "NONE"
+    # prompt with a float cache of another dtype: attention reads the rows in the query dtype
+    separate = not quant and not has_past and np.dtype(cache_dtype) != q.dtype
+    ak = [[[None] * len(pk[b][g]) for g in range(Nkv)] for b in range(B)]
+    av = [[[None] * len(pv[b][g]) for g in range(Nkv)] for b in range(B)]
     int4 = quant and attrs.get("kv_cache_bit_width", 8) == 4
     qmax = 7 if int4 else 127
     eps = attrs.get("qk_norm_epsilon", 1e-6)
@@ -112,6 +116,9 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
                     kr = rope(kr, past + i)
                 pk[b][g][past + i] = store(kr, g, "k_scale")
                 pv[b][g][past + i] = store(vr, g, "v_scale")
+                if separate:
+                    ak[b][g][past + i] = np.array(kr, dtype=np.float64).astype(q.dtype)
+                    av[b][g][past + i] = np.array(vr, dtype=np.float64).astype(q.dtype)
         for h in range(N):
             g = h // G
             for i in range(S):
@@ -129,7 +136,7 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
                         continue
                     if W >= 0 and j < pos - W:
                         continue
-                    kj = value(pk[b][g][j], g, "k_scale")
+                    kj = value(ak[b][g][j] if separate else pk[b][g][j], g, "k_scale")
                     s = scale * math.fsum(qr[d] * kj[d] for d in range(H))
                     if cap > 0:
                         s = cap * math.tanh(s / cap)
@@ -149,7 +156,8 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
                 for d in range(H):
                     terms = []
                     for j, s in logits:
-                        terms.append(math.exp(s - lse) * value(pv[b][g][j], g, "v_scale")[d])
+                        vj = av[b][g][j] if separate else pv[b][g][j]
+                        terms.append(math.exp(s - lse) * value(vj, g, "v_scale")[d])
                     out[b, i, h * H + d] = math.fsum(terms)
     pk_arr = np.array([[np.stack(pk[b][g]) for g in range(Nkv)] for b in range(B)])
     pv_arr = np.array([[np.stack(pv[b][g]) for g in range(Nkv)] for b in range(B)])

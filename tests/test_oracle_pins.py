@@ -51,6 +51,9 @@ BRUTE_CASES = {
     "f16_mha": tiny(dtype="f16", N=2, Nkv=2, mode="shared", S=2, capacity=6, seqlens_k=(3, 5)),
     "bidirectional": tiny(causal=0, seqlens_k=(2, 2)),
     "explicit_scale_g4": tiny(N=8, Nkv=2, scale=0.3, mode="shared", S=1, capacity=5, seqlens_k=(2, 4)),
+    "f16_prompt_f32_cache_rotary": tiny(dtype="f16", S=4, capacity=6, seqlens_k=(3, 2), cache_dtype="f32",
+                                        rotary_theta=1e4, qk_norm=True),
+    "f32_prompt_f16_cache_bidirectional": tiny(S=4, capacity=5, seqlens_k=(3, 3), cache_dtype="f16", causal=0),
     "int4_per_channel_prompt": tiny(S=4, capacity=6, seqlens_k=(3, 2), quant="PER_CHANNEL", bits=4,
                                     scale_range=(0.15, 0.4)),
     "int4_per_tensor_norm_rotary": tiny(S=3, capacity=5, seqlens_k=(2, 2), quant="PER_TENSOR", bits=4,
@@ -424,6 +427,36 @@ def test_int4_prompt_cache_bytes_and_rejects_past():
                       seed=21)
     with pytest.raises(ValueError):
         run(shared)
+
+
+# ---------------------------------------------------------------- prompt cache dtype
+
+@pytest.mark.parametrize("dtype,cache", [("f16", "f32"), ("f32", "f16")])
+def test_prompt_cache_dtype_does_not_change_the_output(dtype, cache):
+    """A prompt's float cache may be float16 or float32 whatever the query dtype
+    (com.microsoft.GroupQueryAttention, section Description): attention is computed
+    from Q/K/V and the cache is written separately, so the output is the same as with
+    a cache of the query dtype and the cache holds the rows rounded to its own dtype."""
+    base = tiny(dtype=dtype, S=5, capacity=7, seqlens_k=(4, 2), rotary_theta=1e4, qk_norm=True)
+    same = run(generate(base, seed=31))
+    case = generate(base.with_(cache_dtype=cache), seed=31)
+    other = run(case)
+    assert np.array_equal(other["output_f64"], same["output_f64"])
+    want = np.float32 if cache == "f32" else np.float16
+    assert other["present_key"].dtype == want
+    for b in range(2):
+        for pos in range(5):
+            np.testing.assert_array_equal(other["present_key"][b, :, pos],
+                                          other["appended_key_f64"][b, :, pos].astype(want))
+    np.testing.assert_array_equal(other["present_key"][:, :, 5:], case["present_key"][:, :, 5:])
+
+
+def test_float_cache_of_another_dtype_with_a_past_is_rejected():
+    case = generate(tiny(dtype="f16", mode="shared", S=1, capacity=4, seqlens_k=(1, 2)), seed=32)
+    case["inputs"]["past_key"] = case["inputs"]["past_key"].astype(np.float32)
+    case["inputs"]["past_value"] = case["inputs"]["past_value"].astype(np.float32)
+    with pytest.raises(ValueError):
+        run(case)
 
 
 # ---------------------------------------------------------------- cache bookkeeping
