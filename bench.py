@@ -403,7 +403,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
         "data": "synthetic (seeded numpy, shapes and distributions of the workload)",
         "config": {"workload": args.workload, "batch": sp.B, "seq_len": sp.S, "num_heads": sp.N,
                    "kv_num_heads": sp.Nkv, "head_size": sp.H, "capacity": sp.capacity,
-                   "cache": (f"{sp.quant} int{sp.bits}" if sp.quant != "NONE" else sp.dtype),
+                   "cache": (f"{sp.quant} int{sp.bits}" if sp.quant != "NONE" else (sp.cache_dtype or sp.dtype)),
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then read back)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "regime": "decode" if plan.regime == 1 else "prefill",

@@ -74,7 +74,7 @@ struct Plan {
   bool tensor_core;  // prefill on the tcgen05 kernel (fp16, head size 128)
   bool tc_decode;    // decode on a tcgen05 kernel (fp16 cache <= 16 rows, or int8 cache with fp32 <= 8 rows; H=128)
   bool tc_i8;        // ... the int8-cache one
-  size_t hdr_bytes, qprep_bytes, part_bytes, total_bytes;
+  size_t hdr_bytes, qprep_bytes, kvsep_bytes, part_bytes, total_bytes;
   size_t part_rows;  // decode partial rows (part_o holds part_rows x H floats, part_ml part_rows x 2)
 };
 
@@ -130,12 +130,18 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
     i4 = a.kv_cache_bit_width == 4;
     cache_dt = i4 ? GQA_U8 : GQA_I8;
   }
-  if (pk.dtype != cache_dt || pv.dtype != cache_dt) {
-    if (!kq && (pk.dtype == GQA_F32 || pk.dtype == GQA_F16))
-      return fail(GQA_ERR_UNSUPPORTED, "a float cache of another dtype than query is not implemented");
-    return fail(GQA_ERR_INVALID_ARGUMENT, "present cache dtype must be %s",
-                i4 ? "uint8 (packed 4-bit codes)" : kq ? "int8" : "the query dtype");
+  // A prompt (no past) may write its float cache as float16 or float32 whatever
+  // the query dtype (section Description); an existing cache has the query dtype.
+  const bool separate = !kq && pk.dtype != q.dtype && (pk.dtype == GQA_F32 || pk.dtype == GQA_F16) &&
+                        pv.dtype == pk.dtype;
+  if (separate) {
+    if (present(in->past_key) || present(in->past_value))
+      return fail(GQA_ERR_INVALID_ARGUMENT, "past_key/past_value must have the query dtype");
+    cache_dt = pk.dtype;
   }
+  if (pk.dtype != cache_dt || pv.dtype != cache_dt)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "present cache dtype must be %s",
+                i4 ? "uint8 (packed 4-bit codes)" : kq ? "int8" : "float16 or float32 (one dtype for K and V)");
   const long long row_w = i4 ? H / 2 : H;   // cache elements per row
   if (pk.ndim != 4 || pk.shape[0] != B || pk.shape[1] != Nkv || pk.shape[3] != row_w)
     return fail(GQA_ERR_INVALID_ARGUMENT, "present_key must be (B, kv_num_heads, C, %s), got %s",
@@ -263,7 +269,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.B = (int)B; P.S = (int)S; P.N = N; P.Nkv = Nkv; P.G = G; P.H = (int)H;
   P.C = (int)C; P.past_cap = (int)past_cap; P.total_len = (int)T; P.mode = mode;
   P.t_type = tdt == GQA_F16 ? gqa::kF16 : gqa::kF32;
-  P.cache_type = i4 ? gqa::kI4 : kq ? gqa::kI8 : P.t_type;
+  P.cache_type = i4 ? gqa::kI4 : kq ? gqa::kI8 : cache_dt == GQA_F16 ? gqa::kF16 : gqa::kF32;
+  P.kv_separate = separate ? 1 : 0;
   P.k_quant = a.k_quant_type; P.v_quant = a.v_quant_type;
   P.causal = a.causal ? 1 : 0;
   P.window = a.local_window_size;
@@ -278,13 +285,15 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.out = out->output.data;
 
   // ---- regime and workspace plan
-  // A 4-bit cache is built by a prompt and always takes the prefill kernels.
-  pl->decode = !i4 && (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P)));
+  // A 4-bit cache is built by a prompt and always takes the prefill kernels, as
+  // does a prompt whose float cache has another dtype than the query.
+  pl->decode = !i4 && !separate && (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P)));
   pl->tc_i8 = pl->decode && gqa::decode_tc_i8_supported(P);
   pl->tc_decode = pl->decode && (gqa::decode_tc_supported(P) || pl->tc_i8);
   pl->tensor_core = false;
   pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));  // status, tickets
   pl->qprep_bytes = 0;
+  pl->kvsep_bytes = 0;
   pl->part_bytes = 0;
   pl->part_rows = 0;
   if (pl->decode) {
@@ -315,8 +324,9 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
     pl->tensor_core = gqa::prefill_tc_supported(P);
     P.qprep_type = pl->tensor_core ? gqa::kF16 : gqa::kF32;
     pl->qprep_bytes = align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
+    if (separate) pl->kvsep_bytes = 2 * align_up((size_t)B * Nkv * S * H * (tdt == GQA_F16 ? 2 : 4));
   }
-  pl->total_bytes = pl->hdr_bytes + pl->qprep_bytes + pl->part_bytes;
+  pl->total_bytes = pl->hdr_bytes + pl->qprep_bytes + pl->kvsep_bytes + pl->part_bytes;
   return GQA_OK;
 }
 
@@ -329,6 +339,11 @@ void bind_workspace(Plan* pl, void* ws) {
   if (pl->qprep_bytes) {
     P.qprep = cur;
     cur += pl->qprep_bytes;
+  }
+  if (pl->kvsep_bytes) {
+    P.kv_sep_k = cur;
+    P.kv_sep_v = cur + pl->kvsep_bytes / 2;
+    cur += pl->kvsep_bytes;
   }
   if (pl->part_bytes) {
     P.part_o = reinterpret_cast<float*>(cur);

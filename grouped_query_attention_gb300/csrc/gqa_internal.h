@@ -22,6 +22,7 @@ struct Params {
   int mode;       // CacheMode
   int t_type;     // ElemType of query/key/value/output (kF32 | kF16)
   int cache_type; // ElemType of the cache (kF32 | kF16 | kI8 | kI4)
+  int kv_separate; // 1: a prompt's float cache of another dtype than T; attention reads kv_sep_k/v
   int k_quant, v_quant;  // gqa_quant values
   // ---- attributes (resolved)
   int causal;
@@ -56,6 +57,8 @@ struct Params {
   unsigned int* status;  // OR of GQA_DEVICE_* bits
   void* qprep;           // prepared queries, layout [B][N_kv][S*G][H]
   int qprep_type;        // ElemType of qprep
+  void* kv_sep_k;        // kv_separate: new K/V rows in T as attention reads them, [B][N_kv][S][H]
+  void* kv_sep_v;
   float* part_o;         // decode partial outputs [B*N_kv][max_splits][R][H]
                          // (tensor-core decode: [max_splits][R][H], one slot per CTA segment)
   float* part_ml;        // decode partial (m, l)   [B*N_kv][max_splits][R][2] (same note)

@@ -74,8 +74,13 @@ prefill_simt_kernel(const Params p) {
   constexpr bool i4 = std::is_same<CacheT, uint8_t>::value;
   constexpr bool i8 = std::is_same<CacheT, int8_t>::value;
   const long long row_elems = i4 ? H / 2 : H;
-  const CacheT* kb = reinterpret_cast<const CacheT*>(p.present_k) + ((long long)b * p.Nkv + g) * p.C * row_elems;
-  const CacheT* vb = reinterpret_cast<const CacheT*>(p.present_v) + ((long long)b * p.Nkv + g) * p.C * row_elems;
+  // Attention reads the present cache, or the new rows in T when a prompt's
+  // cache has another float dtype (kv_separate: [B][N_kv][S][H], S rows).
+  const void* ksrc = p.kv_separate ? p.kv_sep_k : p.present_k;
+  const void* vsrc = p.kv_separate ? p.kv_sep_v : p.present_v;
+  const long long rows = p.kv_separate ? p.S : p.C;
+  const CacheT* kb = reinterpret_cast<const CacheT*>(ksrc) + ((long long)b * p.Nkv + g) * rows * row_elems;
+  const CacheT* vb = reinterpret_cast<const CacheT*>(vsrc) + ((long long)b * p.Nkv + g) * rows * row_elems;
 
   for (int t0 = kmin; t0 < kmax; t0 += kTile) {
     __syncthreads();
@@ -186,15 +191,17 @@ cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st) {
   dim3 grid((nrows + kRows - 1) / kRows, p.Nkv, p.B), block(kWarps * 32);
   const size_t smem = (size_t)(kRows * p.H + 2 * kTile * (p.H + 1)) * sizeof(float);
   cudaError_t e;
+  // With kv_separate the rows attention reads have the query dtype.
+  const int src = p.kv_separate ? p.t_type : p.cache_type;
   if (p.t_type == kF16) {
     e = cudaFuncSetAttribute(prefill_simt_kernel<__half, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prefill_simt_kernel<__half, __half><<<grid, block, smem, st>>>(p);
-  } else if (p.cache_type == kI8) {
+  } else if (src == kI8) {
     e = cudaFuncSetAttribute(prefill_simt_kernel<float, int8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prefill_simt_kernel<float, int8_t><<<grid, block, smem, st>>>(p);
-  } else if (p.cache_type == kI4) {
+  } else if (src == kI4) {
     e = cudaFuncSetAttribute(prefill_simt_kernel<float, uint8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prefill_simt_kernel<float, uint8_t><<<grid, block, smem, st>>>(p);

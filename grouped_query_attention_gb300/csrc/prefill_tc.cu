@@ -253,7 +253,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
   const int qrow0 = bg * nrows + r0;                 // row of Q0 in the prepared-query matrix
-  const int krow0 = bg * p.C + kmin;                 // row of the first key in the cache matrix
+  const int krow0 = bg * (p.kv_separate ? p.S : p.C) + kmin;   // row of the first key in the K/V matrix
 
   if (warp == 0) {
     // ================================================================ TMA producer
@@ -728,17 +728,20 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 }  // namespace
 
 bool prefill_tc_supported(const Params& p) {
-  return p.t_type == kF16 && p.cache_type == kF16 && p.H == kHD;
+  // With kv_separate attention reads the new rows in T (fp16 here).
+  return p.t_type == kF16 && (p.cache_type == kF16 || p.kv_separate) && p.H == kHD;
 }
 
 cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps) {
   const long long qrows = (long long)p.B * p.Nkv * p.S * p.G;
-  const long long krows = (long long)p.B * p.Nkv * p.C;
+  const long long krows = (long long)p.B * p.Nkv * (p.kv_separate ? p.S : p.C);
   cudaError_t e = encode_fp16_2d_sw128(&maps->m[0], p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM);
   if (e != cudaSuccess) return e;
-  if ((e = encode_fp16_2d_sw128(&maps->m[1], p.present_k, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
+  const void* ksrc = p.kv_separate ? p.kv_sep_k : p.present_k;
+  const void* vsrc = p.kv_separate ? p.kv_sep_v : p.present_v;
+  if ((e = encode_fp16_2d_sw128(&maps->m[1], ksrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
     return e;
-  return encode_fp16_2d_sw128(&maps->m[2], p.present_v, (uint64_t)krows, kHD, kHD * 2, 64, kBN);
+  return encode_fp16_2d_sw128(&maps->m[2], vsrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN);
 }
 
 namespace {

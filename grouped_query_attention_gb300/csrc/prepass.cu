@@ -70,11 +70,18 @@ __device__ __forceinline__ void store_n(DstT* dst, const float* src) {
 // Row roles of the flattened row index.
 enum Role { kKey = 0, kValue = 1, kQuery = 2 };
 
+// A prompt's float cache of another dtype than T: attention reads the new rows
+// in T from the workspace (kv_sep_k / kv_sep_v) instead of the cache.
+template <typename T, typename CacheT>
+constexpr bool kSeparate = (std::is_same<CacheT, float>::value || std::is_same<CacheT, __half>::value) &&
+                           !std::is_same<T, CacheT>::value;
+
 // Appends V consecutive values (head coordinates d0 .. d0+V-1 of row pos of KV
 // head `head`) to the present K or V cache: a cast for a float cache, int8
 // codes, or for a 4-bit cache (CacheT = uint8_t) V/2 bytes of +8-biased
-// nibbles with the even coordinate in the low nibble.
-template <typename CacheT, int V>
+// nibbles with the even coordinate in the low nibble. With a separate cache
+// dtype the values are also stored in T for attention.
+template <typename T, typename CacheT, int V>
 __device__ __forceinline__ void append_chunk(const Params& p, int role, int b, int head, int pos, int d0,
                                              const float* y) {
   const int H = p.H;
@@ -101,6 +108,10 @@ __device__ __forceinline__ void append_chunk(const Params& p, int role, int b, i
     else *reinterpret_cast<int2*>(dst) = *reinterpret_cast<int2*>(q4);
   } else {
     store_n<CacheT, V>(reinterpret_cast<CacheT*>(base) + row * H + d0, y);
+  }
+  if constexpr (kSeparate<T, CacheT>) {
+    T* sep = reinterpret_cast<T*>(role == kKey ? p.kv_sep_k : p.kv_sep_v);
+    store_n<T, V>(sep + (((long long)b * p.Nkv + head) * p.S + pos) * H + d0, y);
   }
 }
 
@@ -197,7 +208,7 @@ prepass_kernel(const Params p) {
                 (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
       store_n<QT, V>(dst, y);
     } else {
-      append_chunk<CacheT, V>(p, role, b, head, pos, d0, y);
+      append_chunk<T, CacheT, V>(p, role, b, head, pos, d0, y);
     }
   }
 }
@@ -292,7 +303,7 @@ prepass_vec_kernel(const Params p) {
         QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
         store_n<QT, V>(dst, xr);
       } else {
-        append_chunk<CacheT, V>(p, role, b, head, pos, d0, xr);
+        append_chunk<T, CacheT, V>(p, role, b, head, pos, d0, xr);
       }
     }
   }
@@ -352,9 +363,14 @@ cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
   // Vectorised kernel whenever a row is a power-of-two count (<= 32) of 16-byte chunks.
   bool done = false;
   cudaError_t ev;
-  if (p.t_type == kF16)
+  if (p.t_type == kF16 && p.cache_type == kF32)
+    ev = p.qprep_type == kF16 ? launch_vec<__half, float, __half>(p, st, &done)
+                              : launch_vec<__half, float, float>(p, st, &done);
+  else if (p.t_type == kF16)
     ev = p.qprep_type == kF16 ? launch_vec<__half, __half, __half>(p, st, &done)
                               : launch_vec<__half, __half, float>(p, st, &done);
+  else if (p.cache_type == kF16)
+    ev = launch_vec<float, __half, float>(p, st, &done);
   else if (p.cache_type == kI8)
     ev = launch_vec<float, int8_t, float>(p, st, &done);
   else if (p.cache_type == kI4)
@@ -367,9 +383,14 @@ cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
   if (blocks == 0) return cudaSuccess;
   dim3 grid(blocks), block(kWarpsPerBlock * 32);
   const bool q16 = p.qprep_type == kF16;
-  if (p.t_type == kF16) {
+  if (p.t_type == kF16 && p.cache_type == kF32) {
+    if (q16) prepass_kernel<__half, float, __half><<<grid, block, 0, st>>>(p);
+    else prepass_kernel<__half, float, float><<<grid, block, 0, st>>>(p);
+  } else if (p.t_type == kF16) {
     if (q16) prepass_kernel<__half, __half, __half><<<grid, block, 0, st>>>(p);
     else prepass_kernel<__half, __half, float><<<grid, block, 0, st>>>(p);
+  } else if (p.cache_type == kF16) {
+    prepass_kernel<float, __half, float><<<grid, block, 0, st>>>(p);
   } else if (p.cache_type == kI8) {
     prepass_kernel<float, int8_t, float><<<grid, block, 0, st>>>(p);
   } else if (p.cache_type == kI4) {

@@ -174,9 +174,10 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
 # The synthetic workloads (sizes and distributions of the operator's use
 # cases): a tiny fp32 prompt, fp16 decode over a shared cache, fp16 causal
 # prefill with Q/K RMS norm and rotary, fp16 chunked prefill with window,
-# softcap, head sink, bias and rotary, fp32 decode over an int8 cache, and
-# fp32 prompts that build an int8 or a 4-bit cache (the quantised-cache
-# prefill variants of section Implementation variants).
+# softcap, head sink, bias and rotary, fp32 decode over an int8 cache, an
+# fp16 bidirectional prompt that writes an fp32 cache, and fp32 prompts that
+# build an int8 or a 4-bit cache (the quantised-cache prefill variants of
+# section Implementation variants).
 WORKLOADS = {
     "prompt_f32_b1_s16": CaseSpec(
         name="prompt_f32_b1_s16", dtype="f32", B=1, S=16, N=4, Nkv=2, H=32, capacity=16,
@@ -195,6 +196,9 @@ WORKLOADS = {
     "decode_int8_f32_b32_c16384": CaseSpec(
         name="decode_int8_f32_b32_c16384", dtype="f32", B=32, S=1, N=32, Nkv=8, H=128,
         capacity=16384, mode="shared", seqlens_range=(4096, 16383), quant="PER_CHANNEL"),
+    "prompt_bidirectional_f16_cache_f32_b4_s2048": CaseSpec(
+        name="prompt_bidirectional_f16_cache_f32_b4_s2048", dtype="f16", B=4, S=2048, N=32, Nkv=8, H=128,
+        capacity=2048, mode="prompt", seqlens_k=(2047, 2047, 2047, 2047), causal=0, cache_dtype="f32"),
     "prefill_int8_f32_b2_s2048": CaseSpec(
         name="prefill_int8_f32_b2_s2048", dtype="f32", B=2, S=2048, N=32, Nkv=8, H=128, capacity=2048,
         mode="prompt", seqlens_k=(2047, 2047), quant="PER_CHANNEL"),

@@ -121,6 +121,10 @@ def test_workloads_validate():
     for name, sp in WORKLOADS.items():
         c = FakeCall(dtype=sp.dtype, B=sp.B, S=sp.S, N=sp.N, Nkv=sp.Nkv, H=sp.H, C=sp.capacity,
                      mode=sp.mode, quant=sp.quant if sp.quant != "NONE" else None, bits=sp.bits)
+        if sp.cache_dtype not in (None, sp.dtype):
+            ct = capi.GQA_F32 if sp.cache_dtype == "f32" else capi.GQA_F16
+            c.out.present_key = c.t(ct, (sp.B, sp.Nkv, sp.capacity, sp.H))
+            c.out.present_value = c.t(ct, (sp.B, sp.Nkv, sp.capacity, sp.H))
         assert c.size() > 0, name
 
 
@@ -140,11 +144,13 @@ def test_shape_and_dtype_errors():
     c.inp.k_scale = c.t(capi.GQA_F32, (7,))                               # scale length not 1 / N_kv*H
     _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
     c = FakeCall()
-    c.out.present_key = c.t(capi.GQA_F32, (2, 2, 64, 128))                # float cache of another dtype
+    c.out.present_key = c.t(capi.GQA_F32, (2, 2, 64, 128))                # past of another dtype than query
     c.out.present_value = c.t(capi.GQA_F32, (2, 2, 64, 128))
-    c.inp.past_key = capi.GqaTensor()
-    c.inp.past_value = capi.GqaTensor()
-    _expect(c, capi.GQA_ERR_UNSUPPORTED)
+    c.inp.past_key, c.inp.past_value = c.out.present_key, c.out.present_value
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+    c = FakeCall(mode="prompt", S=4, C=64)
+    c.out.present_key = c.t(capi.GQA_F32, (2, 2, 64, 128))                # K and V caches of two dtypes
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
     c = FakeCall(H=40, N=8)                                               # head size not a multiple of 16
     _expect(c, capi.GQA_ERR_UNSUPPORTED)
 
@@ -182,6 +188,27 @@ def test_optional_input_errors():
     c = FakeCall()
     c.inp.attention_bias = c.t(capi.GQA_F16, (1, 1, 1, 64))               # broadcast dims: fine
     assert c.size() > 0
+
+
+def test_prompt_cache_of_another_float_dtype():
+    """A prompt may write an fp32 cache for fp16 Q/K/V and the reverse; it takes the prefill regime
+    and a workspace copy of the new rows in the query dtype."""
+    for dtype, cache in (("f16", capi.GQA_F32), ("f32", capi.GQA_F16)):
+        for S in (1, 40):
+            c = FakeCall(dtype=dtype, mode="prompt", S=S, C=64)
+            base = c.size()
+            c.out.present_key = c.t(cache, (2, 2, 64, 128))
+            c.out.present_value = c.t(cache, (2, 2, 64, 128))
+            h = capi.gqa_create(capi.make_attrs(**c.attrs))
+            try:
+                info = capi.gqa_describe_plan(h, c.inp, c.out)
+                assert info.regime == capi.GQA_REGIME_PREFILL
+                esize = 2 if dtype == "f16" else 4
+                assert info.workspace_bytes >= 2 * 2 * 2 * S * 128 * esize
+                if S == 40:
+                    assert info.workspace_bytes > base
+            finally:
+                capi.gqa_destroy(h)
 
 
 def test_int4_cache_checks():

@@ -102,6 +102,20 @@ PREFILL = {
     "f16_tc_small_softcap": spec(S=40, N=16, Nkv=2, softcap=1.0, seqlens_range=(40, 700), rotary_theta=1e4),
     "f16_tc_staged_bias_small_softcap": spec(S=64, N=16, Nkv=2, softcap=2.0, bias=(1, 1, 0.5),
                                              local_window_size=200, seqlens_range=(64, 600)),
+    # a prompt's float cache of the other float dtype (attention reads the new rows in the query dtype)
+    "f16_prompt_f32_cache_tc_rotary_norm": spec(S=150, N=8, Nkv=2, mode="prompt", capacity=160,
+                                                seqlens_k=(149, 70, 3), seqlens_range=None, cache_dtype="f32",
+                                                rotary_theta=1e4, qk_norm=True),
+    "f16_prompt_f32_cache_bidirectional_h64": spec(H=64, N=4, Nkv=2, S=33, mode="prompt", capacity=33, causal=0,
+                                                   seqlens_k=(32, 20, 5), seqlens_range=None, cache_dtype="f32"),
+    "f16_prompt_f32_cache_h256_generic_prepass": spec(H=256, N=4, Nkv=2, S=20, mode="prompt", capacity=24,
+                                                      seqlens_k=(19, 19, 10), seqlens_range=None, cache_dtype="f32"),
+    "f32_prompt_f16_cache_s1": spec(dtype="f32", S=1, mode="prompt", capacity=2, seqlens_k=(0, 0, 0),
+                                    seqlens_range=None, cache_dtype="f16"),
+    "f32_prompt_f16_cache_all_features": spec(dtype="f32", N=8, Nkv=2, S=37, mode="prompt", capacity=40,
+                                              seqlens_k=(36, 20, 0), seqlens_range=None, cache_dtype="f16",
+                                              local_window_size=7, softcap=20.0, head_sink=True,
+                                              bias=(3, 8, 0.5)),
     # 4-bit prompt cache (fp32 Q/K/V): packed nibbles written by the pre-pass, unpacked by the prefill
     "i4_per_channel_prompt_padding": spec(dtype="f32", S=37, N=8, Nkv=2, mode="prompt", capacity=40,
                                           seqlens_k=(36, 20, 0), seqlens_range=None, quant="PER_CHANNEL", bits=4,
