@@ -25,6 +25,15 @@ the readings the library implements):
     whatever the query dtype; attention then reads the new K/V rows as they
     would be stored in the query dtype (computed from Q/K/V directly, the
     cache written separately), so the output does not depend on that choice;
+  * sliding_window_cache = 1 with a past cache: the past buffer holds the
+    most recent n_old = min(past_b, L) rows of the sequence (L its capacity),
+    oldest first; the present keeps the last n_new - S of them at rows
+    0 .. n_new-S-1 (evicted from the front, compacted) and appends the S new
+    rows after them, n_new = min(n_old + S, C); cache row r then holds
+    absolute position total_b - n_new + r, which masks, bias columns and
+    rotary use. Requires causal attention, local_window_size W > 0,
+    C >= S + W and L >= W, so every key a query can see is kept. Without a
+    past cache the flag changes nothing;
   * RMS norm y = x / sqrt(mean(x^2) + eps) * w, weight used as given;
   * padding rows of a prompt (i >= total_b, no past) produce a zero output row;
     their K/V rows are still appended.
@@ -204,7 +213,7 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
     Returns output (dtype of query), output_f64, present_key/value, and the
     fp64 values of the appended rows before the storage cast
     (appended_key_f64 / appended_value_f64, (B, N_kv, S, H)) with their
-    cache positions (appended_pos, (B, S)).
+    cache rows (appended_pos, (B, S)).
 
     com.microsoft.GroupQueryAttention: section Description (grouped-query
     attention over BSH Q/K/V and BNSH caches), sections Inputs / Outputs /
@@ -270,6 +279,15 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
     bias = None if inputs.get("attention_bias") is None else np.asarray(inputs["attention_bias"])
     sink = inputs.get("head_sink")
     smooth = int(a["smooth_softmax"]) == 1
+    # Window-shift cache (section Attributes, sliding_window_cache; section
+    # Implementation variants, window_shift: compact the surviving rows, append
+    # the chunk, enforce the window floor and the causal bound).
+    window_cache = int(a["sliding_window_cache"]) == 1
+    if window_cache:
+        if not causal or W <= 0:
+            raise ValueError("sliding_window_cache needs causal attention and local_window_size > 0")
+        if has_past and (C < S + W or np.asarray(past_k).shape[2] < W):
+            raise ValueError("a window cache needs capacity >= S + local_window_size and a past of >= W rows")
 
     wanted = None
     if sample is not None:
@@ -284,14 +302,29 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
     for b in range(B):
         total_b = int(seqlens[b]) + 1
         past_b = total_b - S if has_past else 0
-        if total_b < 1 or total_b > total_len or past_b < 0 or past_b + S > C or total_b > C:
-            raise ValueError(f"batch {b}: seqlens_k inconsistent with the cache")
-        pos = past_b + np.arange(S)
+        win = window_cache and has_past
+        if win:
+            if total_b < S or total_b > total_len:
+                raise ValueError(f"batch {b}: seqlens_k inconsistent with the cache")
+            n_old = min(past_b, np.asarray(past_k).shape[2])
+            n_live = min(n_old + S, C)            # cache rows after the update
+            keep = n_live - S                     # past rows that survive, most recent first kept
+        else:
+            if total_b < 1 or total_b > total_len or past_b < 0 or past_b + S > C or total_b > C:
+                raise ValueError(f"batch {b}: seqlens_k inconsistent with the cache")
+            n_live, keep = total_b, past_b
+        off = total_b - n_live                    # absolute position of cache row 0
+        pos = past_b + np.arange(S)               # absolute positions of the new rows
+        rows_new = keep + np.arange(S)            # their cache rows
 
-        # Cache update. Copy mode keeps the live past rows; then the S new rows
-        # are appended at positions past_b .. past_b+S-1 (K: norm, then rotary,
-        # then cast or int8 code; V: cast or int8 code).
-        if has_past and not share_buffer:
+        # Cache update. Copy mode keeps the live past rows; a window cache keeps
+        # the most recent `keep` of them at the front; then the S new rows are
+        # appended at rows keep .. keep+S-1 (K: norm, then rotary at the
+        # absolute position, then cast or int8 code; V: cast or int8 code).
+        if win:
+            pk[b, :, :keep] = np.asarray(past_k)[b, :, n_old - keep:n_old]
+            pv[b, :, :keep] = np.asarray(past_v)[b, :, n_old - keep:n_old]
+        elif has_past and not share_buffer:
             pk[b, :, :past_b] = np.asarray(past_k)[b, :, :past_b]
             pv[b, :, :past_b] = np.asarray(past_v)[b, :, :past_b]
         for g in range(Nkv):
@@ -301,17 +334,17 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 kr = rms_norm(kr, kw, eps)
             if rotary:
                 kr = rotary_neox(kr, cos_c[pos], sin_c[pos])
-            pk[b, g, pos] = _store(kr, pk.dtype, kq, k_scale, g, H, bits)
-            pv[b, g, pos] = _store(vr, pv.dtype, vq, v_scale, g, H, bits)
+            pk[b, g, rows_new] = _store(kr, pk.dtype, kq, k_scale, g, H, bits)
+            pv[b, g, rows_new] = _store(vr, pv.dtype, vq, v_scale, g, H, bits)
             if separate:   # the rows attention reads: the query dtype
-                attn_k[b, g, pos] = kr.astype(out_dtype)
-                attn_v[b, g, pos] = vr.astype(out_dtype)
+                attn_k[b, g, rows_new] = kr.astype(out_dtype)
+                attn_v[b, g, rows_new] = vr.astype(out_dtype)
             new_k[b, g], new_v[b, g] = kr, vr
-        new_pos[b] = pos
+        new_pos[b] = rows_new
 
-        # Attention of every live query row over cache rows 0 .. total_b-1 as stored.
+        # Attention of every live query row over cache rows 0 .. n_live-1 as stored.
         live_rows = S if has_past else min(S, total_b)
-        j = np.arange(total_b)
+        j = off + np.arange(n_live)               # absolute positions of cache rows 0 .. n_live-1
         for h in range(N):
             if wanted is not None and (b, h) not in wanted:
                 continue
@@ -321,19 +354,19 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
                 if rows.size == 0:
                     continue
             g = h // G if head_of_group == "block" else h % Nkv
-            kd = _load(attn_k[b, g, :total_b], kq, k_scale, g, H, bits)
-            vd = _load(attn_v[b, g, :total_b], vq, v_scale, g, H, bits)
+            kd = _load(attn_k[b, g, :n_live], kq, k_scale, g, H, bits)
+            vd = _load(attn_v[b, g, :n_live], vq, v_scale, g, H, bits)
             qr = q_in[b, rows, h * H:(h + 1) * H].astype(np.float64)
             if qw is not None:
                 qr = rms_norm(qr, qw, eps)
             if rotary:
                 qr = rotary_neox(qr, cos_c[pos[rows]], sin_c[pos[rows]])
-            s = scale * (qr @ kd.T)                      # (rows, total_b)
+            s = scale * (qr @ kd.T)                      # (rows, n_live)
             if bias_after_softcap:
                 s = softcap_scores(s, softcap)
             if bias is not None:
                 bb = bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0]
-                s = s + bb[rows, :total_b].astype(np.float64)
+                s = s + bb[rows][:, j].astype(np.float64)
             if not bias_after_softcap:
                 s = softcap_scores(s, softcap)
             p = pos[rows][:, None]

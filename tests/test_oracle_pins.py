@@ -459,6 +459,75 @@ def test_float_cache_of_another_dtype_with_a_past_is_rejected():
         run(case)
 
 
+# ---------------------------------------------------------------- sliding-window cache
+
+def _window_pair(S, W, L, C, totals, seed, share=True, rotary=True, bias=True):
+    """The same call twice: over a full-history cache (no eviction) and over a
+    window buffer holding the most recent rows of the same history."""
+    big = max(totals) + 4
+    spec = tiny(mode="shared", S=S, capacity=big, seqlens_k=tuple(t - 1 for t in totals), local_window_size=W,
+                rotary_theta=1e4 if rotary else None, rotary_rows=big, bias=(2, 1, 0.5) if bias else None)
+    full = generate(spec, seed=seed)
+    inp = dict(full["inputs"])
+    B, Nkv, H = 2, 2, 8
+    dt = inp["past_key"].dtype
+    win_k = np.zeros((B, Nkv, L, H), dt) + 7
+    win_v = np.zeros((B, Nkv, L, H), dt) - 7
+    for b, t in enumerate(totals):
+        past = t - S
+        n_old = min(past, L)
+        win_k[b, :, :n_old] = inp["past_key"][b, :, past - n_old:past]
+        win_v[b, :, :n_old] = inp["past_value"][b, :, past - n_old:past]
+    attrs = dict(full["attrs"], sliding_window_cache=1)
+    if share:
+        inp_w = dict(inp, past_key=win_k, past_value=win_v)
+        res_w = oracle.gqa_forward(inp_w, attrs, None, None, True)
+    else:
+        inp_w = dict(inp, past_key=win_k, past_value=win_v)
+        pres_k = np.zeros((B, Nkv, C, H), dt) + 3
+        pres_v = np.zeros((B, Nkv, C, H), dt) - 3
+        res_w = oracle.gqa_forward(inp_w, attrs, pres_k, pres_v, False)
+    res_full = oracle.gqa_forward(inp, full["attrs"], None, None, True)
+    return res_full, res_w
+
+
+@pytest.mark.parametrize("S,W,L,C,totals,share", [
+    (1, 3, 4, 4, (9, 3), True),        # decode: full buffer evicts one row; short history no eviction
+    (2, 2, 5, 5, (12, 6), True),       # chunk of two rows
+    (3, 2, 4, 6, (10, 4), False),      # separate past (4 rows) and present (6 rows)
+])
+def test_window_cache_equals_full_history(S, W, L, C, totals, share):
+    """Evicting keys that no query can see (window W, capacity >= S + W) changes
+    nothing: the output equals attention over the full history, and the window
+    buffer holds the most recent rows of the full cache, oldest first
+    (com.microsoft.GroupQueryAttention, section Attributes, sliding_window_cache)."""
+    full, win = _window_pair(S, W, L, C if not share else L, totals, seed=41, share=share)
+    np.testing.assert_allclose(win["output_f64"], full["output_f64"], rtol=1e-12, atol=1e-14)
+    cap = win["present_key"].shape[2]
+    for b, t in enumerate(totals):
+        n_live = min(min(t - S, L) + S, cap)
+        np.testing.assert_array_equal(win["present_key"][b, :, :n_live], full["present_key"][b, :, t - n_live:t])
+        np.testing.assert_array_equal(win["present_value"][b, :, :n_live], full["present_value"][b, :, t - n_live:t])
+
+
+def test_window_cache_flag_without_past_changes_nothing():
+    spec = tiny(S=4, capacity=6, seqlens_k=(3, 2), local_window_size=2)
+    case = generate(spec, seed=42)
+    a = run(case)
+    b = oracle.gqa_forward(case["inputs"], dict(case["attrs"], sliding_window_cache=1), case["present_key"],
+                           case["present_value"])
+    assert np.array_equal(a["output_f64"], b["output_f64"])
+    assert np.array_equal(a["present_key"], b["present_key"])
+
+
+def test_window_cache_rejects_bad_settings():
+    case = generate(tiny(mode="shared", S=1, capacity=4, seqlens_k=(5, 2), local_window_size=3), seed=43)
+    for over in (dict(local_window_size=-1), dict(local_window_size=0), dict(local_window_size=4),
+                 dict(causal=0, local_window_size=-1)):
+        with pytest.raises(ValueError):
+            oracle.gqa_forward(case["inputs"], dict(case["attrs"], sliding_window_cache=1, **over), None, None, True)
+
+
 # ---------------------------------------------------------------- cache bookkeeping
 
 def test_non_appended_rows_unchanged_shared_and_prompt():
