@@ -360,7 +360,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": ["decode_tc.cu", "decode_tc_i8.cu", "tcgen05.cuh"],
                   "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
-                  "copy_past": ["prepass.cu"]}[dominant]
+                  "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"]}[dominant]
     peak_key = "hbm_gbs" if wk["bound"] == "hbm" else "bf16_tflops"
     if wk["bound"] == "hbm":
         achieved = wk["kv_bytes"] / (dom_ms / 1e3) / 1e9

@@ -170,9 +170,14 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
       if (past_cap != C) return fail(GQA_ERR_INVALID_ARGUMENT, "a shared past/present buffer must have one capacity");
       mode = gqa::kShared;
     } else {
-      if (C != past_cap + S) return fail(GQA_ERR_INVALID_ARGUMENT, "present length must be past length + S when not shared");
+      if (C != past_cap + S && !a.sliding_window_cache)
+        return fail(GQA_ERR_INVALID_ARGUMENT, "present length must be past length + S when not shared");
       mode = gqa::kCopy;
     }
+    if (a.sliding_window_cache && (C < S + a.local_window_size || past_cap < a.local_window_size))
+      return fail(GQA_ERR_INVALID_ARGUMENT,
+                  "a window cache needs capacity >= S + local_window_size (%lld < %lld) and a past of >= %d rows", C,
+                  S + a.local_window_size, a.local_window_size);
     if (!a.causal) return fail(GQA_ERR_UNSUPPORTED, "bidirectional attention over a past cache is not implemented");
   } else if (C < S) {
     return fail(GQA_ERR_INVALID_ARGUMENT, "present capacity %lld is smaller than sequence_length %lld", C, S);
@@ -186,7 +191,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   if (T < 1) return fail(GQA_ERR_INVALID_ARGUMENT, "total_sequence_length must be >= 1");
   if (mode == gqa::kPrompt && T > S)
     return fail(GQA_ERR_INVALID_ARGUMENT, "without a past cache total_sequence_length (%lld) cannot exceed S (%lld)", T, S);
-  if (T > C)
+  const bool window = a.sliding_window_cache == 1 && mode != gqa::kPrompt;   // window-shift update
+  if (T > C && !window)
     return fail(GQA_ERR_INVALID_ARGUMENT, "total_sequence_length (%lld) exceeds the present capacity (%lld)", T, C);
 
   // ---- optional inputs
@@ -271,6 +277,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.t_type = tdt == GQA_F16 ? gqa::kF16 : gqa::kF32;
   P.cache_type = i4 ? gqa::kI4 : kq ? gqa::kI8 : cache_dt == GQA_F16 ? gqa::kF16 : gqa::kF32;
   P.kv_separate = separate ? 1 : 0;
+  P.window_cache = window ? 1 : 0;
   P.k_quant = a.k_quant_type; P.v_quant = a.v_quant_type;
   P.causal = a.causal ? 1 : 0;
   P.window = a.local_window_size;
@@ -287,7 +294,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   // ---- regime and workspace plan
   // A 4-bit cache is built by a prompt and always takes the prefill kernels, as
   // does a prompt whose float cache has another dtype than the query.
-  pl->decode = !i4 && !separate && (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P)));
+  // A window cache takes the pre-pass and the CUDA-core prefill for every shape.
+  pl->decode = !i4 && !separate && !window && (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P)));
   pl->tc_i8 = pl->decode && gqa::decode_tc_i8_supported(P);
   pl->tc_decode = pl->decode && (gqa::decode_tc_supported(P) || pl->tc_i8);
   pl->tensor_core = false;
@@ -321,7 +329,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   } else {
     if (!gqa::prefill_simt_supported(P) || !gqa::prepass_supported(P))
       return fail(GQA_ERR_UNSUPPORTED, "no prefill kernel for head_size %lld", H);
-    pl->tensor_core = gqa::prefill_tc_supported(P);
+    pl->tensor_core = !window && gqa::prefill_tc_supported(P);
     P.qprep_type = pl->tensor_core ? gqa::kF16 : gqa::kF32;
     pl->qprep_bytes = align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
     if (separate) pl->kvsep_bytes = 2 * align_up((size_t)B * Nkv * S * H * (tdt == GQA_F16 ? 2 : 4));
@@ -409,7 +417,10 @@ gqa_status gqa_create(const gqa_attrs* a, gqa_handle** out) {
     return fail(GQA_ERR_INVALID_ARGUMENT, "scale/softcap/qk_norm_epsilon must be finite, softcap and epsilon >= 0");
   for (int qt : {a->k_quant_type, a->v_quant_type})
     if (qt < GQA_QUANT_NONE || qt > GQA_QUANT_PER_CHANNEL) return fail(GQA_ERR_INVALID_ARGUMENT, "unknown quant type %d", qt);
-  if (a->sliding_window_cache == 1) return fail(GQA_ERR_UNSUPPORTED, "sliding_window_cache is not implemented");
+  if (a->sliding_window_cache != 0 && a->sliding_window_cache != 1)
+    return fail(GQA_ERR_INVALID_ARGUMENT, "sliding_window_cache must be 0 or 1");
+  if (a->sliding_window_cache == 1 && (a->causal != 1 || a->local_window_size <= 0))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "sliding_window_cache needs causal attention and local_window_size > 0");
   if (a->k_quant_type != GQA_QUANT_NONE && a->kv_cache_bit_width != 8 && a->kv_cache_bit_width != 4)
     return fail(GQA_ERR_INVALID_ARGUMENT, "kv_cache_bit_width must be 8 or 4");
   gqa_handle* h = new (std::nothrow) gqa_handle;
@@ -439,7 +450,7 @@ gqa_status gqa_describe_plan(const gqa_handle* h, const gqa_inputs* in, const gq
   gqa_status s = plan_call(h, in, out, &pl);
   if (s != GQA_OK) return s;
   info->regime = pl.decode ? GQA_REGIME_DECODE : GQA_REGIME_PREFILL;
-  info->launches = (pl.P.mode == gqa::kCopy ? 1 : 0) + (pl.decode ? 1 : 2);
+  info->launches = (pl.P.mode == gqa::kCopy || pl.P.window_cache ? 1 : 0) + (pl.decode ? 1 : 2);
   info->split_len = pl.decode ? pl.P.split_len : 0;
   info->max_splits = pl.decode ? pl.P.max_splits : 0;
   info->workspace_bytes = pl.total_bytes;
@@ -471,7 +482,10 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   else if (!pl.decode && pl.tensor_core)
     e = gqa::prepare_prefill_tc(P, &maps);
   if (e != cudaSuccess) return cuda_fail(e, "TMA tensor maps");
-  if (P.mode == gqa::kCopy) {
+  if (P.window_cache) {
+    e = timed_launch(h, GQA_KERNEL_WINDOW_SHIFT, st, [&] { return gqa::launch_window_shift(P, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "window shift of the cache");
+  } else if (P.mode == gqa::kCopy) {
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }

@@ -23,6 +23,7 @@ struct Params {
   int t_type;     // ElemType of query/key/value/output (kF32 | kF16)
   int cache_type; // ElemType of the cache (kF32 | kF16 | kI8 | kI4)
   int kv_separate; // 1: a prompt's float cache of another dtype than T; attention reads kv_sep_k/v
+  int window_cache; // 1: sliding_window_cache with a past cache (window-shift update, see batch_rows)
   int k_quant, v_quant;  // gqa_quant values
   // ---- attributes (resolved)
   int causal;
@@ -71,12 +72,43 @@ struct Params {
 // Batch-level data check shared by all kernels: returns past_b (rows already
 // cached) or -1 if seqlens_k[b] is inconsistent with the shapes.
 __host__ __device__ inline int batch_past(const Params& p, int total) {
-  if (total < 1 || total > p.total_len || total > p.C) return -1;
+  if (total < 1 || total > p.total_len || (total > p.C && !p.window_cache)) return -1;
   if (p.mode == kPrompt) return total <= p.S ? 0 : -1;
   int past = total - p.S;
   if (past < 0) return -1;
-  if (p.mode == kCopy && past > p.past_cap) return -1;
+  if (p.mode == kCopy && past > p.past_cap && !p.window_cache) return -1;
   return past;
+}
+
+// Cache rows of one batch entry. Without a window cache, row r holds absolute
+// position r: the new rows start at row past and rows [0, total) are live.
+// With a window cache (sliding_window_cache = 1 and a past cache) the past
+// buffer holds the most recent n_old = min(past, L) rows (L its capacity);
+// the present keeps the last keep = live - S of them at rows 0 .. keep-1 and
+// the new rows follow, live = min(n_old + S, C); row r holds absolute position
+// off + r, off = total - live.
+struct BatchRows {
+  int keep;  // cache row of the first new row
+  int live;  // live cache rows after the update
+  int off;   // absolute position of cache row 0
+  int n_old; // live rows of the past buffer before the update
+};
+
+__host__ __device__ inline BatchRows batch_rows(const Params& p, int total, int past) {
+  BatchRows r;
+  if (p.window_cache) {
+    const int L = p.mode == kShared ? p.C : p.past_cap;
+    r.n_old = past < L ? past : L;
+    r.live = r.n_old + p.S < p.C ? r.n_old + p.S : p.C;
+    r.keep = r.live - p.S;
+    r.off = total - r.live;
+  } else {
+    r.n_old = past;
+    r.keep = past;
+    r.live = total;
+    r.off = 0;
+  }
+  return r;
 }
 
 // Size of the fixed scratch array behind gqa_forward_noalloc (16 MiB).
@@ -86,6 +118,7 @@ cudaError_t noalloc_scratch(void** ptr);
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_copy_past(const Params& p, cudaStream_t st);
+cudaError_t launch_window_shift(const Params& p, cudaStream_t st);
 cudaError_t launch_prepass(const Params& p, cudaStream_t st);
 cudaError_t launch_decode(const Params& p, cudaStream_t st);
 // TMA tensor maps of a tensor-core launch, encoded on the host before the

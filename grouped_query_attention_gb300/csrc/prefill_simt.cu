@@ -54,12 +54,15 @@ prefill_simt_kernel(const Params p) {
     const int r = r0 + x / H;
     qs[x] = r < nrows ? qp[(long long)r * H + x % H] : 0.f;
   }
-  // Key range of the block: [kmin, kmax).
+  // Key range of the block in cache rows: [kmin, kmax). Cache row j holds
+  // absolute position off + j (off = 0 except for a sliding-window cache).
+  const BatchRows br = batch_rows(p, total, past);
+  const int off = br.off, past_row = past - off;
   const int i_lo = r0 / p.G;
   const int i_hi = min((min(r0 + kRows, nrows) - 1) / p.G, live_i - 1);
-  int kmin = 0, kmax = total;
-  if (p.causal) kmax = min(total, past + i_hi + 1);
-  if (p.window >= 0) kmin = max(0, past + i_lo - p.window);
+  int kmin = 0, kmax = br.live;
+  if (p.causal) kmax = min(br.live, past_row + i_hi + 1);
+  if (p.window >= 0) kmin = max(0, past_row + i_lo - p.window);
 
   const float qscale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
   float m[kRowsPerWarp], l[kRowsPerWarp], o[kRowsPerWarp][kMaxH / 32];
@@ -116,7 +119,7 @@ prefill_simt_kernel(const Params p) {
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
       const int rl = warp * kRowsPerWarp + rr, r = r0 + rl;
       if (r >= nrows) continue;                     // warp-uniform
-      const int i = r / p.G, h = g * p.G + r % p.G, pos = past + i;
+      const int i = r / p.G, h = g * p.G + r % p.G, pos = past_row + i;   // position in cache rows
       if (i >= live_i) continue;
       float s = 0.f;
       for (int d = 0; d < H; ++d) s += qs[rl * H + d] * ks[lane * HP + d];
@@ -127,7 +130,7 @@ prefill_simt_kernel(const Params p) {
       if (p.softcap > 0.f) s = p.softcap * tanhf(s / p.softcap) * kLog2e;
       if (p.has_bias && vis) {
         const long long bi = (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) *
-                                  p.S + i) * p.bias_ld + j;
+                                  p.S + i) * p.bias_ld + j + off;
         s += load_t(p.bias, bi, p.t_type) * kLog2e;
       }
       s = vis ? s : kNegBig;

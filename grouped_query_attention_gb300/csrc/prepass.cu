@@ -76,7 +76,7 @@ template <typename T, typename CacheT>
 constexpr bool kSeparate = (std::is_same<CacheT, float>::value || std::is_same<CacheT, __half>::value) &&
                            !std::is_same<T, CacheT>::value;
 
-// Appends V consecutive values (head coordinates d0 .. d0+V-1 of row pos of KV
+// Appends V consecutive values (head coordinates d0 .. d0+V-1 of cache row pos of KV
 // head `head`) to the present K or V cache: a cast for a float cache, int8
 // codes, or for a 4-bit cache (CacheT = uint8_t) V/2 bytes of +8-biased
 // nibbles with the even coordinate in the low nibble. With a separate cache
@@ -149,7 +149,8 @@ prepass_kernel(const Params p) {
     if (role == kKey && i == 0 && head == 0 && lane == 0) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
     return;
   }
-  const int pos = past + i;
+  const int pos = past + i;                                 // absolute position (rotary)
+  const int crow = batch_rows(p, total, past).keep + i;     // cache row
   const bool rotate = p.has_rotary && role != kValue;
   if (rotate && pos >= p.rotary_rows) {
     if (lane == 0) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
@@ -208,7 +209,7 @@ prepass_kernel(const Params p) {
                 (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
       store_n<QT, V>(dst, y);
     } else {
-      append_chunk<T, CacheT, V>(p, role, b, head, pos, d0, y);
+      append_chunk<T, CacheT, V>(p, role, b, head, crow, d0, y);
     }
   }
 }
@@ -258,7 +259,8 @@ prepass_vec_kernel(const Params p) {
       if (i == 0 && threadIdx.x == 0 && r0 == grp) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
       return;   // the whole block (one token) is skipped
     }
-    const int pos = past + i;
+    const int pos = past + i;                                 // absolute position (rotary)
+    const int crow = batch_rows(p, total, past).keep + i;     // cache row
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int r = r0 + u * GROUPS;
@@ -303,7 +305,7 @@ prepass_vec_kernel(const Params p) {
         QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
         store_n<QT, V>(dst, xr);
       } else {
-        append_chunk<T, CacheT, V>(p, role, b, head, pos, d0, xr);
+        append_chunk<T, CacheT, V>(p, role, b, head, crow, d0, xr);
       }
     }
   }
@@ -353,7 +355,56 @@ __global__ void copy_past_kernel(const Params p, int esize) {
   }
 }
 
+// Window-shift update of a sliding-window cache: present rows [0, keep) =
+// past rows [n_old - keep, n_old) (the most recent ones; the older rows are
+// evicted from the front). One CTA per (batch, KV head, K or V) moves the rows
+// in order, 16-byte vectors, a chunk of kShiftVec vectors per thread at a
+// time: each chunk is read completely before any of it is written, and a
+// chunk's destination lies below the source of every later chunk, so the
+// in-place move of a shared buffer (toward the front) is safe.
+constexpr int kShiftThreads = 256, kShiftVec = 8;
+
+__global__ void __launch_bounds__(kShiftThreads) window_shift_kernel(const Params p, int esize) {
+  const int bg = blockIdx.x, b = bg / p.Nkv;
+  const bool is_v = blockIdx.y == 1;
+  const int total = p.seqlens[b] + 1;
+  const int past = batch_past(p, total);
+  if (past < 0) return;   // the pre-pass reports the bad length
+  const BatchRows r = batch_rows(p, total, past);
+  const int src0 = r.n_old - r.keep;
+  if (r.keep <= 0 || (p.mode == kShared && src0 == 0)) return;   // nothing moves
+  const long long row_bytes = (long long)p.H * esize;
+  const int L = p.mode == kShared ? p.C : p.past_cap;
+  const char* src = reinterpret_cast<const char*>(is_v ? p.past_v : p.past_k) + ((long long)bg * L + src0) * row_bytes;
+  char* dst = reinterpret_cast<char*>(is_v ? p.present_v : p.present_k) + (long long)bg * p.C * row_bytes;
+  const uint4* s16 = reinterpret_cast<const uint4*>(src);
+  uint4* d16 = reinterpret_cast<uint4*>(dst);
+  const long long n16 = (long long)r.keep * row_bytes / 16;
+  for (long long base = 0; base < n16; base += kShiftThreads * kShiftVec) {
+    uint4 v[kShiftVec];
+#pragma unroll
+    for (int k = 0; k < kShiftVec; ++k) {
+      const long long x = base + k * kShiftThreads + threadIdx.x;
+      if (x < n16) v[k] = s16[x];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kShiftVec; ++k) {
+      const long long x = base + k * kShiftThreads + threadIdx.x;
+      if (x < n16) d16[x] = v[k];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_window_shift(const Params& p, cudaStream_t st) {
+  const int esize = p.cache_type == kF32 ? 4 : (p.cache_type == kF16 ? 2 : 1);
+  dim3 grid(p.B * p.Nkv, 2), block(kShiftThreads);
+  window_shift_kernel<<<grid, block, 0, st>>>(p, esize);
+  return cudaGetLastError();
+}
 
 bool prepass_supported(const Params& p) {
   return p.H % 16 == 0 && p.H <= kMaxH && p.H >= 16;

@@ -64,6 +64,7 @@ class CaseSpec:
     quant: str = "NONE"                # NONE | PER_TENSOR | PER_CHANNEL (quantised cache)
     bits: int = 8                      # 8: int8 codes; 4: two 4-bit codes per byte (prompt only)
     cache_dtype: str | None = None     # float cache dtype of a prompt ("f16" / "f32"); None: the query dtype
+    sliding_window_cache: int = 0      # 1: past/present are window buffers (evict from the front)
     scale_range: tuple = (0.005, 0.02)
     extra: dict = field(default_factory=dict)
 
@@ -166,7 +167,7 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
                  local_window_size=spec.local_window_size, scale=spec.scale, softcap=spec.softcap,
                  qk_norm_epsilon=spec.qk_norm_epsilon, smooth_softmax=spec.smooth_softmax,
                  k_quant_type=spec.quant, v_quant_type=spec.quant, kv_cache_bit_width=spec.bits,
-                 sliding_window_cache=0)
+                 sliding_window_cache=spec.sliding_window_cache)
     return dict(inputs=inp, attrs=attrs, present_key=present_k, present_value=present_v,
                 share_buffer=share, spec=spec)
 
@@ -175,7 +176,8 @@ def generate(spec: CaseSpec, seed: int = 0) -> dict:
 # cases): a tiny fp32 prompt, fp16 decode over a shared cache, fp16 causal
 # prefill with Q/K RMS norm and rotary, fp16 chunked prefill with window,
 # softcap, head sink, bias and rotary, fp32 decode over an int8 cache, an
-# fp16 bidirectional prompt that writes an fp32 cache, and fp32 prompts that
+# fp16 bidirectional prompt that writes an fp32 cache, fp16 decode over a
+# sliding-window cache (4096 rows, window 4000), and fp32 prompts that
 # build an int8 or a 4-bit cache (the quantised-cache prefill variants of
 # section Implementation variants).
 WORKLOADS = {
@@ -199,6 +201,10 @@ WORKLOADS = {
     "prompt_bidirectional_f16_cache_f32_b4_s2048": CaseSpec(
         name="prompt_bidirectional_f16_cache_f32_b4_s2048", dtype="f16", B=4, S=2048, N=32, Nkv=8, H=128,
         capacity=2048, mode="prompt", seqlens_k=(2047, 2047, 2047, 2047), causal=0, cache_dtype="f32"),
+    "decode_window_f16_b16_c4096": CaseSpec(
+        name="decode_window_f16_b16_c4096", dtype="f16", B=16, S=1, N=32, Nkv=8, H=128, capacity=4096,
+        mode="shared", seqlens_range=(6000, 12000), rotary_theta=1e4, local_window_size=4000,
+        sliding_window_cache=1),
     "prefill_int8_f32_b2_s2048": CaseSpec(
         name="prefill_int8_f32_b2_s2048", dtype="f32", B=2, S=2048, N=32, Nkv=8, H=128, capacity=2048,
         mode="prompt", seqlens_k=(2047, 2047), quant="PER_CHANNEL"),

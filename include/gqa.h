@@ -88,7 +88,7 @@ typedef struct gqa_attrs {
   int32_t k_quant_type;         /* gqa_quant; NONE (default) */
   int32_t v_quant_type;         /* gqa_quant; NONE (default) */
   int32_t kv_cache_bit_width;   /* 8: int8 cache; 4: packed 4-bit cache (prompt only); ignored when not quantised */
-  int32_t sliding_window_cache; /* 0 (default); 1 is UNSUPPORTED */
+  int32_t sliding_window_cache; /* 0 (default); 1: past/present are window buffers (see gqa_outputs) */
 } gqa_attrs;
 
 /* Inputs, section Inputs of the operator page (same names, same shapes):
@@ -119,6 +119,15 @@ typedef struct gqa_inputs {
 /* Outputs, section Outputs: output T (B, S, N*H); present_key/value T_CACHE
  * (B, N_kv, C, H). Shared buffer: present.data == past.data and C == L.
  * Copy mode: C == L + S. No past: C >= S (a capacity buffer).
+ * sliding_window_cache == 1 with a past cache (section Attributes): the past
+ * buffer (capacity L) holds the most recent n_old = min(past_b, L) rows of
+ * the sequence, oldest first; the present keeps the last n_new - S of them at
+ * rows 0 .. n_new-S-1 (older rows are evicted from the front) and appends the
+ * S new rows after them, n_new = min(n_old + S, C); row r holds absolute
+ * position total_b - n_new + r (masks and bias columns use it; rotary uses
+ * the absolute position). Needs causal = 1, local_window_size W > 0,
+ * C >= S + W and, for a separate past, L >= W; C need not equal L + S and
+ * total_sequence_length may exceed C. Without a past the flag changes nothing.
  * 4-bit cache (kv_cache_bit_width == 4, section Inputs past_key / present_key):
  * GQA_U8 of shape (B, N_kv, C, H/2); byte k of a row holds code(2k) + 8 in
  * its low nibble and code(2k+1) + 8 in its high nibble, code =
@@ -138,7 +147,8 @@ GQA_API void gqa_attrs_default(gqa_attrs* attrs);
  * num_heads % kv_num_heads != 0, causal == 0 with local_window_size != -1,
  * local_window_size < -1, softcap < 0, a non-finite scale or epsilon, or a
  * quant type outside gqa_quant, or a quantised cache whose kv_cache_bit_width
- * is neither 8 nor 4; UNSUPPORTED for sliding_window_cache == 1. */
+ * is neither 8 nor 4, or sliding_window_cache not 0 / 1, or 1 without causal
+ * attention and local_window_size > 0. */
 GQA_API gqa_status gqa_create(const gqa_attrs* attrs, gqa_handle** out);
 
 /* Bytes of device workspace gqa_forward needs for these shapes (host-only;
@@ -242,6 +252,7 @@ GQA_API gqa_status gqa_describe_plan(const gqa_handle* handle, const gqa_inputs*
 #define GQA_KERNEL_PREFILL_CUDA_CORE 4
 #define GQA_KERNEL_PREFILL_TENSOR_CORE 5
 #define GQA_KERNEL_DECODE_TENSOR_CORE 6
+#define GQA_KERNEL_WINDOW_SHIFT 7
 GQA_API gqa_status gqa_profile_begin(gqa_handle* handle, int32_t max_launches);
 GQA_API gqa_status gqa_profile_end(gqa_handle* handle, int32_t* kinds, float* ms, int32_t capacity, int32_t* count);
 

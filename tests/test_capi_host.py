@@ -52,7 +52,9 @@ def test_attrs_defaults_match_page():
     (dict(num_heads=4, kv_num_heads=2, local_window_size=-2), capi.GQA_ERR_INVALID_ARGUMENT),
     (dict(num_heads=4, kv_num_heads=2, softcap=-1.0), capi.GQA_ERR_INVALID_ARGUMENT),
     (dict(num_heads=4, kv_num_heads=2, k_quant_type=7), capi.GQA_ERR_INVALID_ARGUMENT),
-    (dict(num_heads=4, kv_num_heads=2, sliding_window_cache=1), capi.GQA_ERR_UNSUPPORTED),
+    (dict(num_heads=4, kv_num_heads=2, sliding_window_cache=1), capi.GQA_ERR_INVALID_ARGUMENT),   # no window
+    (dict(num_heads=4, kv_num_heads=2, sliding_window_cache=1, local_window_size=0), capi.GQA_ERR_INVALID_ARGUMENT),
+    (dict(num_heads=4, kv_num_heads=2, sliding_window_cache=2, local_window_size=8), capi.GQA_ERR_INVALID_ARGUMENT),
     (dict(num_heads=4, kv_num_heads=2, k_quant_type=2, v_quant_type=2, kv_cache_bit_width=5),
      capi.GQA_ERR_INVALID_ARGUMENT),
 ])
@@ -121,6 +123,8 @@ def test_workloads_validate():
     for name, sp in WORKLOADS.items():
         c = FakeCall(dtype=sp.dtype, B=sp.B, S=sp.S, N=sp.N, Nkv=sp.Nkv, H=sp.H, C=sp.capacity,
                      mode=sp.mode, quant=sp.quant if sp.quant != "NONE" else None, bits=sp.bits)
+        if sp.sliding_window_cache:
+            c.attrs.update(sliding_window_cache=1, local_window_size=sp.local_window_size)
         if sp.cache_dtype not in (None, sp.dtype):
             ct = capi.GQA_F32 if sp.cache_dtype == "f32" else capi.GQA_F16
             c.out.present_key = c.t(ct, (sp.B, sp.Nkv, sp.capacity, sp.H))
@@ -231,6 +235,31 @@ def test_int4_cache_checks():
     _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
     c = FakeCall(dtype="f32", S=4, C=8, mode="prompt", quant="PER_CHANNEL")
     _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, kv_cache_bit_width=4)     # int8 buffers, 4-bit attribute
+
+
+def test_window_cache_checks():
+    """sliding_window_cache: capacity >= S + W (and a separate past of >= W rows); the
+    present need not be past + S; total_sequence_length may exceed the capacity;
+    the window-shift launch comes before the pre-pass and the CUDA-core prefill."""
+    w = dict(sliding_window_cache=1, local_window_size=16)
+    c = FakeCall(S=1, C=64)
+    c.inp.total_sequence_length = 1000
+    assert c.size(**w) > 0
+    h = capi.gqa_create(capi.make_attrs(**{**c.attrs, **w}))
+    try:
+        info = capi.gqa_describe_plan(h, c.inp, c.out)
+        assert info.regime == capi.GQA_REGIME_PREFILL and info.launches == 3
+    finally:
+        capi.gqa_destroy(h)
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, sliding_window_cache=1, local_window_size=64)   # C < S + W
+    c = FakeCall(S=2, C=40, mode="copy")
+    c.inp.past_key = c.t(capi.GQA_F16, (2, 2, 40, 128))                   # present = past, not past + S
+    c.inp.past_value = c.t(capi.GQA_F16, (2, 2, 40, 128))
+    assert c.size(**w) > 0
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)                               # without the window flag
+    c.inp.past_key = c.t(capi.GQA_F16, (2, 2, 8, 128))                    # past shorter than the window
+    c.inp.past_value = c.t(capi.GQA_F16, (2, 2, 8, 128))
+    _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, **w)
 
 
 def test_total_length_beyond_capacity_rejected():

@@ -38,6 +38,17 @@ DECODE = {
                                   rotary_theta=1e4),
     "f32_g1_bias_shared": spec(dtype="f32", N=2, Nkv=2, bias=(1, 1, 0.5), seqlens_range=(0, 300)),
     "f16_long_many_splits": spec(B=2, capacity=6000, seqlens_range=(3000, 5999)),
+    # sliding-window cache: rows evicted from the front, compacted in place, new rows appended
+    "f16_window_cache_decode": spec(S=1, capacity=300, seqlens_range=(250, 900), local_window_size=200,
+                                    sliding_window_cache=1, rotary_theta=1e4),
+    "i8_window_cache_decode": spec(dtype="f32", quant="PER_CHANNEL", capacity=200, seqlens_range=(100, 700),
+                                   local_window_size=150, sliding_window_cache=1),
+    "f32_window_cache_chunk_copy": spec(dtype="f32", S=5, mode="copy", past_len=150, seqlens_range=(10, 700),
+                                        local_window_size=100, sliding_window_cache=1, bias=(3, 1, 0.5),
+                                        softcap=20.0),
+    "f16_window_cache_g8_chunk": spec(S=16, N=16, Nkv=2, capacity=400, seqlens_range=(16, 1500),
+                                      local_window_size=300, sliding_window_cache=1, qk_norm=True,
+                                      rotary_theta=1e4, head_sink=True),
     "f16_window_zero": spec(local_window_size=0),
     "f32_bidirectional_prompt": spec(dtype="f32", mode="prompt", capacity=1, S=1, N=4, Nkv=1, causal=0,
                                      seqlens_k=(0, 0, 0), seqlens_range=None),
