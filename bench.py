@@ -357,7 +357,8 @@ def run_gpu_arm(args, world, rank, local) -> None:
     e2e_value = units_all / (e2e_ms / 1e3)
 
     peaks, peaks_src = load_peaks()
-    kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": ["decode_tc.cu", "decode_tc_i8.cu", "tcgen05.cuh"],
+    tc_decode_src = ["decode_tc_i8.cu" if sp.quant != "NONE" else "decode_tc.cu", "tcgen05.cuh"]
+    kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": tc_decode_src,
                   "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
                   "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"]}[dominant]
