@@ -66,6 +66,23 @@ def visible_pairs(case) -> tuple[int, int]:
     return pairs, kv_rows
 
 
+def window_shift_bytes(case) -> int:
+    """Bytes the window shift of a sliding-window cache reads and writes (K and V):
+    the kept rows min(n_old + S, C) - S move unless they are already at the front."""
+    sp, inp = case["spec"], case["inputs"]
+    S, C = sp.S, sp.capacity
+    L = C if sp.mode == "shared" else sp.past_len
+    esize = 1 if sp.quant != "NONE" else (2 if sp.dtype == "f16" else 4)
+    moved = 0
+    for b in range(sp.B):
+        past = int(inp["seqlens_k"][b]) + 1 - S
+        n_old = min(past, L)
+        keep = min(n_old + S, C) - S
+        if sp.mode != "shared" or n_old - keep > 0:
+            moved += keep
+    return 2 * 2 * moved * sp.Nkv * sp.H * esize
+
+
 def work(case) -> dict:
     sp = case["spec"]
     pairs, kv_rows = visible_pairs(case)
@@ -363,7 +380,14 @@ def run_gpu_arm(args, world, rank, local) -> None:
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
                   "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"]}[dominant]
     peak_key = "hbm_gbs" if wk["bound"] == "hbm" else "bf16_tflops"
-    if wk["bound"] == "hbm":
+    if dominant == "window_shift":
+        # The window shift of a sliding-window cache: bytes of the rows it moves, read and written.
+        wk["bound"] = "hbm"
+        achieved = window_shift_bytes(case) / (dom_ms / 1e3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        peak_key = "hbm_gbs"
+        unit = "GB/s"
+    elif wk["bound"] == "hbm":
         achieved = wk["kv_bytes"] / (dom_ms / 1e3) / 1e9
         peak = float(peaks["hbm_gbs"])
         unit = "GB/s"

@@ -70,7 +70,8 @@ struct DItem {
   int cfirst;            // first CTA of (b, g)
   int j0, jend;          // keys of this segment: [j0, jend)
   int last;              // the segment holds the last tile of (b, g)
-  int past, total, ntiles, end;
+  int past, total, ntiles, end;   // past / total in cache rows (see batch_tiles)
+  int off;                        // absolute position of cache row 0 (rotary, bias columns)
 };
 
 struct __align__(1024) DSmem {
@@ -151,9 +152,10 @@ __device__ __forceinline__ uint32_t sw_elem(uint32_t row, uint32_t col, uint32_t
 
 // Tiles of batch b (its key range [kstart, total) in 128-key tiles, for each
 // KV head); 0 for a batch whose lengths are inconsistent.
-__device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, int& total, bool flag_bad) {
+__device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, int& total, int& off, bool flag_bad) {
   total = p.seqlens[b] + 1;
   past = batch_past(p, total);
+  off = 0;
   if (past >= 0 && p.has_rotary && past + p.S > p.rotary_rows) {
     if (flag_bad) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
     past = -1;
@@ -161,6 +163,12 @@ __device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, in
     flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
   }
   if (past < 0) return 0;
+  // From here on in cache rows: a sliding-window cache keeps the most recent
+  // rows at the front (row r holds absolute position off + r); else off = 0.
+  const BatchRows br = batch_rows(p, total, past);
+  off = br.off;
+  past = br.keep;
+  total = br.live;
   const int kstart = p.window >= 0 ? max(0, past - p.window) : 0;
   return (total - kstart + kKT - 1) / kKT;
 }
@@ -177,8 +185,8 @@ __device__ long long count_units(const Params& p, bool flag_bad) {
   const int lane = threadIdx.x & 31;
   long long n = 0;
   for (int b = lane; b < p.B; b += 32) {
-    int past, total;
-    n += bg_units(batch_tiles(p, b, past, total, flag_bad)) * p.Nkv;
+    int past, total, off;
+    n += bg_units(batch_tiles(p, b, past, total, off, flag_bad)) * p.Nkv;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
@@ -202,8 +210,8 @@ __device__ void map_segment(const Params& p, long long t, long long tend, long l
   long long base = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
     const int b = b0 + lane;
-    int past = -1, total = 0, tb = 0;
-    if (b < p.B) tb = batch_tiles(p, b, past, total, false);
+    int past = -1, total = 0, off = 0, tb = 0;
+    if (b < p.B) tb = batch_tiles(p, b, past, total, off, false);
     const long long n = bg_units(tb) * p.Nkv;
     long long incl = n;
 #pragma unroll
@@ -233,6 +241,7 @@ __device__ void map_segment(const Params& p, long long t, long long tend, long l
       const int kstart = p.window >= 0 ? max(0, pp - p.window) : 0;
       it.past = pp;
       it.total = tt;
+      it.off = __shfl_sync(0xffffffffu, off, src);
       it.j0 = kstart + lt * kKT;
       it.jend = min(tt, kstart + (int)(seg_end - first) * kKT);
       it.ntiles = (int)(seg_end - t);
@@ -324,7 +333,7 @@ __device__ void prepare_qt(const Params& p, const DItem& it, uint8_t* qt) {
     const uint4 xh = *reinterpret_cast<const uint4*>(src + 64 + 8 * l8);
     uint4 cs, sn;
     if (p.has_rotary) {
-      const long long cb = (long long)(it.past + i) * (kHD / 2) + 8 * l8;
+      const long long cb = (long long)(it.past + it.off + i) * (kHD / 2) + 8 * l8;   // absolute position
       cs = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.cos_c) + cb);
       sn = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.sin_c) + cb);
     }
@@ -365,7 +374,7 @@ __device__ void append_rows(const Params& p, const DItem& it) {
     uint4 cs, sn;
     const bool rope = is_k && p.has_rotary;
     if (rope) {
-      const long long cb = (long long)j * (kHD / 2) + 8 * l8;
+      const long long cb = (long long)(j + it.off) * (kHD / 2) + 8 * l8;   // absolute position
       cs = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.cos_c) + cb);
       sn = *reinterpret_cast<const uint4*>(reinterpret_cast<const __half*>(p.sin_c) + cb);
     }
@@ -726,7 +735,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
               const int i = ih_r[r] / p.N, h = ih_r[r] % p.N;
               const long long bi =
                   (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
-                      p.bias_ld + jk;
+                      p.bias_ld + jk + it.off;
               x += load_t(p.bias, bi, p.t_type) * kLog2e;
             }
             s[r] = vis ? x : -INFINITY;

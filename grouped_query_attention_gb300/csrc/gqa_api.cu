@@ -294,8 +294,11 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   // ---- regime and workspace plan
   // A 4-bit cache is built by a prompt and always takes the prefill kernels, as
   // does a prompt whose float cache has another dtype than the query.
-  // A window cache takes the pre-pass and the CUDA-core prefill for every shape.
-  pl->decode = !i4 && !separate && !window && (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P)));
+  // A window cache takes the tensor-core decode kernels (which work in cache
+  // rows with an absolute offset) or else the pre-pass and the CUDA-core prefill.
+  pl->decode = !i4 && !separate &&
+               (window ? (gqa::decode_tc_supported(P) || gqa::decode_tc_i8_supported(P))
+                       : (gqa::decode_supported(P) || (S * G <= 16 && gqa::decode_tc_supported(P))));
   pl->tc_i8 = pl->decode && gqa::decode_tc_i8_supported(P);
   pl->tc_decode = pl->decode && (gqa::decode_tc_supported(P) || pl->tc_i8);
   pl->tensor_core = false;
@@ -527,7 +530,10 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
   if (pl.tc_decode &&
       (e = pl.tc_i8 ? gqa::prepare_decode_tc_i8(P, &maps) : gqa::prepare_decode_tc(P, &maps)) != cudaSuccess)
     return cuda_fail(e, "TMA tensor maps");
-  if (P.mode == gqa::kCopy) {
+  if (P.window_cache) {
+    e = timed_launch(h, GQA_KERNEL_WINDOW_SHIFT, st, [&] { return gqa::launch_window_shift(P, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "window shift of the cache");
+  } else if (P.mode == gqa::kCopy) {
     e = timed_launch(h, GQA_KERNEL_COPY_PAST, st, [&] { return gqa::launch_copy_past(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "copy of past rows");
   }

@@ -240,17 +240,20 @@ def test_int4_cache_checks():
 def test_window_cache_checks():
     """sliding_window_cache: capacity >= S + W (and a separate past of >= W rows); the
     present need not be past + S; total_sequence_length may exceed the capacity;
-    the window-shift launch comes before the pre-pass and the CUDA-core prefill."""
+    the window-shift launch comes first, then the tensor-core decode (fp16, H=128,
+    S*G <= 16) or the pre-pass and the CUDA-core prefill."""
     w = dict(sliding_window_cache=1, local_window_size=16)
+    for S, regime, launches in ((1, capi.GQA_REGIME_DECODE, 2), (8, capi.GQA_REGIME_PREFILL, 3)):
+        c = FakeCall(S=S, C=64)
+        c.inp.total_sequence_length = 1000
+        assert c.size(**w) > 0
+        h = capi.gqa_create(capi.make_attrs(**{**c.attrs, **w}))
+        try:
+            info = capi.gqa_describe_plan(h, c.inp, c.out)
+            assert info.regime == regime and info.launches == launches
+        finally:
+            capi.gqa_destroy(h)
     c = FakeCall(S=1, C=64)
-    c.inp.total_sequence_length = 1000
-    assert c.size(**w) > 0
-    h = capi.gqa_create(capi.make_attrs(**{**c.attrs, **w}))
-    try:
-        info = capi.gqa_describe_plan(h, c.inp, c.out)
-        assert info.regime == capi.GQA_REGIME_PREFILL and info.launches == 3
-    finally:
-        capi.gqa_destroy(h)
     _expect(c, capi.GQA_ERR_INVALID_ARGUMENT, sliding_window_cache=1, local_window_size=64)   # C < S + W
     c = FakeCall(S=2, C=40, mode="copy")
     c.inp.past_key = c.t(capi.GQA_F16, (2, 2, 40, 128))                   # present = past, not past + S

@@ -46,6 +46,11 @@ DECODE = {
     "f32_window_cache_chunk_copy": spec(dtype="f32", S=5, mode="copy", past_len=150, seqlens_range=(10, 700),
                                         local_window_size=100, sliding_window_cache=1, bias=(3, 1, 0.5),
                                         softcap=20.0),
+    "f16_window_cache_tc_all_features": spec(S=2, N=16, Nkv=2, capacity=300, seqlens_range=(200, 900),
+                                             local_window_size=250, sliding_window_cache=1, bias=(3, 1, 0.5),
+                                             softcap=30.0, rotary_theta=1e4, qk_norm=True, head_sink=True),
+    "f16_window_cache_copy_decode": spec(S=1, mode="copy", past_len=300, seqlens_range=(100, 900),
+                                         local_window_size=250, sliding_window_cache=1, rotary_theta=1e4),
     "f16_window_cache_g8_chunk": spec(S=16, N=16, Nkv=2, capacity=400, seqlens_range=(16, 1500),
                                       local_window_size=300, sliding_window_cache=1, qk_norm=True,
                                       rotary_theta=1e4, head_sink=True),
