@@ -83,7 +83,7 @@ struct __align__(1024) DSmem {
   float redl[4][kNR];           // cross-warp row sum
   DItem item[2];
   uint64_t kfull[kNS], kempty[kNS], vfull[kNS], vempty[kNS];
-  uint64_t imap[2], iready[2], iempty[2];
+  uint64_t imap[2], qready[2], iready[2], iempty[2];   // item mapped / query rows / appended rows / slot free
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full;
   uint64_t drain;
@@ -451,6 +451,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.imap[s], 1);
+      mbar_init(&sm.qready[s], 1);
       mbar_init(&sm.iready[s], 1);
       mbar_init(&sm.iempty[s], 2);  // MMA commit (Q^T reads done) + softmax release
       mbar_init(&sm.s_full[s], 1);
@@ -506,6 +507,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         if (lane == 0) {
           sm.item[slot].end = 1;
           mbar_arrive(&sm.imap[slot]);
+          mbar_arrive(&sm.qready[slot]);
           mbar_arrive(&sm.iready[slot]);
         }
         break;
@@ -522,8 +524,11 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         mbar_arrive(&sm.imap[slot]);
       }
       prepare_qt(p, it, sm.qt[slot]);
+      fence_async_smem();   // query rows (shared) -> async proxy: the MMAs may start
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.qready[slot]);
       append_rows(p, it);
-      fence_async_all();  // query rows (shared) and appended rows (global) -> async proxy
+      fence_async_all();  // appended rows (global) -> async proxy: the TMA may load their tile
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.iready[slot]);
       iphase[slot] ^= 1u;
@@ -624,7 +629,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       return true;
     };
     while (ok) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot]))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.qready[slot], iphase[slot]))) {
         ok = false;
         break;
       }
@@ -680,7 +685,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     int slot = 0, tau = 0, icount = 0;
     uint32_t iphase[2] = {0, 0};
     while (true) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.qready[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
       named_sync();
       if (aborted(sm)) break;
       const DItem it = sm.item[slot];
@@ -865,19 +870,53 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
             Ls[r] = 0.f;
             A[r] = 0.f;
           }
-          for (int s2 = 0; s2 < it.nsplit; ++s2) {
-            const long long sb0 = (long long)(s2 == 0 ? it.slot0 : 2 * (it.cfirst + s2)) * p.rows_pad;
+          if constexpr (R > 4) {
+            for (int s2 = 0; s2 < it.nsplit; ++s2) {
+              const long long sb0 = (long long)(s2 == 0 ? it.slot0 : 2 * (it.cfirst + s2)) * p.rows_pad;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-              if (r >= rows) continue;
-              const float m = __ldcg(&p.part_ml[(sb0 + r) * 2]);
-              const float l = __ldcg(&p.part_ml[(sb0 + r) * 2 + 1]);
-              const float ov = __ldcg(&p.part_o[(sb0 + r) * kHD + kl]);
-              const float mn = fmaxf(M[r], m);
-              const float fa = ex2(M[r] - mn), fb = ex2(m - mn);
-              Ls[r] = Ls[r] * fa + l * fb;
-              A[r] = A[r] * fa + ov * fb;
-              M[r] = mn;
+              for (int r = 0; r < R; ++r) {
+                if (r >= rows) continue;
+                const float m = __ldcg(&p.part_ml[(sb0 + r) * 2]);
+                const float l = __ldcg(&p.part_ml[(sb0 + r) * 2 + 1]);
+                const float ov = __ldcg(&p.part_o[(sb0 + r) * kHD + kl]);
+                const float mn = fmaxf(M[r], m);
+                const float fa = ex2(M[r] - mn), fb = ex2(m - mn);
+                Ls[r] = Ls[r] * fa + l * fb;
+                A[r] = A[r] * fa + ov * fb;
+                M[r] = mn;
+              }
+            }
+          } else {
+            // Up to four rows: four splits per pass, their loads issued before any
+            // is combined; more rows: one split per pass (register budget).
+            constexpr int kMB = 4;
+            for (int s0 = 0; s0 < it.nsplit; s0 += kMB) {
+              float mv[kMB][R], lv[kMB][R], ovv[kMB][R];
+#pragma unroll
+              for (int k = 0; k < kMB; ++k) {
+                const int s2 = min(s0 + k, it.nsplit - 1);   // a repeated split is not combined
+                const long long sb0 = (long long)(s2 == 0 ? it.slot0 : 2 * (it.cfirst + s2)) * p.rows_pad;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  if (r >= rows) continue;
+                  mv[k][r] = __ldcg(&p.part_ml[(sb0 + r) * 2]);
+                  lv[k][r] = __ldcg(&p.part_ml[(sb0 + r) * 2 + 1]);
+                  ovv[k][r] = __ldcg(&p.part_o[(sb0 + r) * kHD + kl]);
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < kMB; ++k) {
+                if (s0 + k >= it.nsplit) break;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                  if (r >= rows) continue;
+                  const float mn = fmaxf(M[r], mv[k][r]);
+                  const float fa = ex2(M[r] - mn), fb = ex2(mv[k][r] - mn);
+                  Ls[r] = Ls[r] * fa + lv[k][r] * fb;
+                  A[r] = A[r] * fa + ovv[k][r] * fb;
+                  M[r] = mn;
+                }
+              }
             }
           }
 #pragma unroll
