@@ -378,7 +378,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": tc_decode_src,
                   "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
-                  "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"]}[dominant]
+                  "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"], "bias_stage": ["prepass.cu"]}[dominant]
     peak_key = "hbm_gbs" if wk["bound"] == "hbm" else "bf16_tflops"
     if dominant == "window_shift":
         # The window shift of a sliding-window cache: bytes of the rows it moves, read and written.

@@ -27,7 +27,7 @@ EXPORTS = ["gqa_attrs_default", "gqa_create", "gqa_workspace_size", "gqa_forward
            "gqa_read_device_status", "gqa_describe_plan", "gqa_destroy", "gqa_status_string",
            "gqa_last_error", "gqa_forward_noalloc", "gqa_profile_begin", "gqa_profile_end"]
 KERNEL_KINDS = {1: "copy_past", 2: "prepass", 3: "decode", 4: "prefill_cuda_core", 5: "prefill_tensor_core",
-                6: "decode_tensor_core", 7: "window_shift"}
+                6: "decode_tensor_core", 7: "window_shift", 8: "bias_stage"}
 GQA_REGIME_DECODE, GQA_REGIME_PREFILL = 1, 2
 
 

@@ -74,7 +74,8 @@ struct Plan {
   bool tensor_core;  // prefill on the tcgen05 kernel (fp16, head size 128)
   bool tc_decode;    // decode on a tcgen05 kernel (fp16 cache <= 16 rows, or int8 cache with fp32 <= 8 rows; H=128)
   bool tc_i8;        // ... the int8-cache one
-  size_t hdr_bytes, qprep_bytes, kvsep_bytes, part_bytes, total_bytes;
+  size_t hdr_bytes, qprep_bytes, kvsep_bytes, bias_bytes, part_bytes, total_bytes;
+  bool bias_staged;  // tensor-core prefill with the bias staged by a small kernel and copied by TMA
   size_t part_rows;  // decode partial rows (part_o holds part_rows x H floats, part_ml part_rows x 2)
 };
 
@@ -305,6 +306,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));  // status, tickets
   pl->qprep_bytes = 0;
   pl->kvsep_bytes = 0;
+  pl->bias_bytes = 0;
+  pl->bias_staged = false;
   pl->part_bytes = 0;
   pl->part_rows = 0;
   if (pl->decode) {
@@ -336,8 +339,13 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
     P.qprep_type = pl->tensor_core ? gqa::kF16 : gqa::kF32;
     pl->qprep_bytes = align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
     if (separate) pl->kvsep_bytes = 2 * align_up((size_t)B * Nkv * S * H * (tdt == GQA_F16 ? 2 : 4));
+    if (pl->tensor_core && gqa::prefill_tc_bias_staged(P)) {
+      pl->bias_staged = true;
+      P.bias_stage_ld = (int)((P.bias_ld + 3) & ~3);   // 16-byte rows for the tensor copies
+      pl->bias_bytes = align_up((size_t)P.bias_bdim * S * P.bias_stage_ld * sizeof(float));
+    }
   }
-  pl->total_bytes = pl->hdr_bytes + pl->qprep_bytes + pl->kvsep_bytes + pl->part_bytes;
+  pl->total_bytes = pl->hdr_bytes + pl->qprep_bytes + pl->kvsep_bytes + pl->bias_bytes + pl->part_bytes;
   return GQA_OK;
 }
 
@@ -355,6 +363,10 @@ void bind_workspace(Plan* pl, void* ws) {
     P.kv_sep_k = cur;
     P.kv_sep_v = cur + pl->kvsep_bytes / 2;
     cur += pl->kvsep_bytes;
+  }
+  if (pl->bias_bytes) {
+    P.bias_stage = reinterpret_cast<float*>(cur);
+    cur += pl->bias_bytes;
   }
   if (pl->part_bytes) {
     P.part_o = reinterpret_cast<float*>(cur);
@@ -453,7 +465,7 @@ gqa_status gqa_describe_plan(const gqa_handle* h, const gqa_inputs* in, const gq
   gqa_status s = plan_call(h, in, out, &pl);
   if (s != GQA_OK) return s;
   info->regime = pl.decode ? GQA_REGIME_DECODE : GQA_REGIME_PREFILL;
-  info->launches = (pl.P.mode == gqa::kCopy || pl.P.window_cache ? 1 : 0) + (pl.decode ? 1 : 2);
+  info->launches = (pl.P.mode == gqa::kCopy || pl.P.window_cache ? 1 : 0) + (pl.decode ? 1 : 2) + (pl.bias_staged ? 1 : 0);
   info->split_len = pl.decode ? pl.P.split_len : 0;
   info->max_splits = pl.decode ? pl.P.max_splits : 0;
   info->workspace_bytes = pl.total_bytes;
@@ -499,6 +511,10 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   } else {
     e = timed_launch(h, GQA_KERNEL_PREPASS, st, [&] { return gqa::launch_prepass(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "pre-pass launch");
+    if (pl.bias_staged) {
+      e = timed_launch(h, GQA_KERNEL_BIAS_STAGE, st, [&] { return gqa::launch_bias_stage(P, st); });
+      if (e != cudaSuccess) return cuda_fail(e, "bias staging launch");
+    }
     if (pl.tensor_core)
       e = timed_launch(h, GQA_KERNEL_PREFILL_TENSOR_CORE, st, [&] { return gqa::launch_prefill_tc(P, st, maps); });
     else

@@ -58,6 +58,8 @@ struct Params {
   unsigned int* status;  // OR of GQA_DEVICE_* bits
   void* qprep;           // prepared queries, layout [B][N_kv][S*G][H]
   int qprep_type;        // ElemType of qprep
+  float* bias_stage;     // bias * log2(e) as fp32 rows of bias_stage_ld floats ([bdim*S] rows) for the
+  int bias_stage_ld;     // tensor-core prefill's TMA bias staging (16-byte row stride), else null
   void* kv_sep_k;        // kv_separate: new K/V rows in T as attention reads them, [B][N_kv][S][H]
   void* kv_sep_v;
   float* part_o;         // decode partial outputs [B*N_kv][max_splits][R][H]
@@ -124,8 +126,12 @@ cudaError_t launch_decode(const Params& p, cudaStream_t st);
 // TMA tensor maps of a tensor-core launch, encoded on the host before the
 // launch (kept out of the launch itself so nothing but the launch sits
 // between a caller's timing events).
+cudaError_t launch_bias_stage(const Params& p, cudaStream_t st);
+// Whether the tensor-core prefill stages the bias (shared by all heads, G >= 8) by TMA.
+bool prefill_tc_bias_staged(const Params& p);
+
 struct TmaMaps {
-  CUtensorMap m[3];
+  CUtensorMap m[4];
 };
 cudaError_t prepare_decode_tc(const Params& p, TmaMaps* maps);
 cudaError_t launch_decode_tc(const Params& p, cudaStream_t st, const TmaMaps& maps);

@@ -13,11 +13,12 @@
 //                live-length masks, softcap, bias, online max with lazy
 //                rescaling of O in tensor memory, P written back over S as
 //                fp16, epilogue O / l (+ sink term) to the output.
-//                With a bias shared by all heads (G >= 8) warp 0 also stages
+//                With a bias shared by all heads (G >= 8) warp 0 also copies
 //                the bias block of each key tile (the CTA's distinct query
-//                positions x 128 keys, fp32 times log2(e)) into a 2-stage
-//                shared-memory ring with coalesced loads, so the softmax
-//                threads read it with 16-byte shared loads.
+//                positions x 128 keys of the fp32 bias * log2(e) that a small
+//                kernel stages before the launch) into a 2-stage shared ring
+//                with one tensor copy; the softmax threads read it with
+//                16-byte shared loads.
 // The two softmax groups ping-pong: while one works on its tile the tensor
 // core runs the other's MMAs. Tensor memory: S0 | S1 | O0 | O1 (512 columns).
 // Every barrier wait is bounded; on expiry the CTA sets the TIMEOUT status
@@ -44,6 +45,7 @@ constexpr int kBN = 128;                        // keys per K/V tile
 constexpr int kHD = 128;                        // head size
 constexpr int kNS = 2;                          // K/V stages
 constexpr int kBiasRows = 33;                   // staged bias rows (distinct query positions of a CTA, G >= 8)
+constexpr uint32_t kBiasBytes = kBiasRows * 128 * 4;   // one staged bias box (fp32)
 
 // Kernel variants: scores without softcap and bias; softcap and/or bias read
 // by each softmax thread; bias staged in shared memory by a loader warp.
@@ -185,7 +187,7 @@ __device__ __forceinline__ void set_abort(const Params& p, TcSmem& sm) {
 template <int MODE, bool CAP>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
 prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmb) {
   constexpr bool PLAIN = MODE == kPlain;
   constexpr bool STAGED = MODE == kStagedBias;
   constexpr int kThreads = threads_for(MODE);
@@ -240,7 +242,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     }
     if constexpr (STAGED) {
       for (int s = 0; s < kNS; ++s) {
-        mbar_init(&sm.bias_full[s], 32);          // every loader lane
+        mbar_init(&sm.bias_full[s], 1);           // the TMA warp's elected lane (with the copy's bytes)
         mbar_init(&sm.bias_empty[s], 8);          // one lane of every softmax warp
       }
     }
@@ -258,27 +260,17 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
   if (warp == 0) {
     // ================================================================ TMA producer
     // The whole warp waits; one elected lane issues. With a staged bias the
-    // warp then loads the bias block of the same key tile: stage s holds
-    // bias[bb, 0, i_lo + rho, j0 .. j0+127] * log2(e) in fp32 for the CTA's
-    // positions rho = 0 .. nbr-1, and -inf where key j0+col is not visible
-    // from position past + i_lo + rho (beyond the live length, causal bound,
-    // window floor): the visibility mask of every head at that position, so
-    // the softmax threads add it and need no mask of their own. Lane l moves
-    // the key pairs (2l, 2l+1) and (64+2l, 65+2l) of each row; the loads of
-    // 17 rows are issued before any of them is stored.
-    const int nbr = STAGED ? min(i_hi - i_lo + 1, kBiasRows) : 0;   // the host checks the span fits
-    const unsigned short* bias0 =
-        STAGED ? reinterpret_cast<const unsigned short*>(p.bias) + ((long long)(p.bias_bdim > 1 ? b : 0) * p.S + i_lo) * p.bias_ld
-               : nullptr;
-    const int T = p.bias_ld;
-    constexpr int kRowsPerBatch = 17;
+    // warp then loads the bias block of the same key tile with one tensor
+    // copy: stage s holds the staged bias rows bb*S + i_lo .. +kBiasRows-1
+    // (fp32 times log2(e)), keys j0 .. j0+127; keys past the bias row read 0.
+    const int brow0 = STAGED ? (p.bias_bdim > 1 ? b : 0) * p.S + i_lo : 0;
     if (elect_one()) {
       mbar_arrive_tx(&sm.q_full, 2 * kTile);
       for (int q = 0; q < 2; ++q)
         for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.q[q] + bx * kBox, &tmq, bx * 64, qrow0 + q * kBM, &sm.q_full);
     }
     __syncwarp();
-    int issued = 0;
+    int issued = 0, issued_b = 0;
     for (int t = 0; t < ntiles; ++t) {
       const int st = t % kNS;
       const uint32_t ph = (uint32_t)(t / kNS) & 1u;
@@ -300,51 +292,18 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           if (lane == 0) set_abort(p, sm);
           break;
         }
-        const int j0 = kmin + t * kBN;
-        const int ja = j0 + 2 * lane, jb = j0 + 64 + 2 * lane;
-        // Unconditional loads at clamped (in-bounds) positions, selected after:
-        // no branch separates the loads, so all of a batch are in flight at once.
-        const int ka0 = min(ja, T - 1), ka1 = min(ja + 1, T - 1), kb0 = min(jb, T - 1), kb1 = min(jb + 1, T - 1);
-        const uint32_t ma0 = ja < T ? 0xffffu : 0u, ma1 = ja + 1 < T ? 0xffffu : 0u;
-        const uint32_t mb0 = jb < T ? 0xffffu : 0u, mb1 = jb + 1 < T ? 0xffffu : 0u;
-        for (int base = 0; base < nbr; base += kRowsPerBatch) {
-          uint32_t a[kRowsPerBatch], c[kRowsPerBatch];   // two fp16 bit patterns each, low = even key
-#pragma unroll
-          for (int k = 0; k < kRowsPerBatch; ++k) {
-            const unsigned short* src = bias0 + (long long)min(base + k, nbr - 1) * T;
-            a[k] = ((uint32_t)__ldg(src + ka0) & ma0) | (((uint32_t)__ldg(src + ka1) & ma1) << 16);
-            c[k] = ((uint32_t)__ldg(src + kb0) & mb0) | (((uint32_t)__ldg(src + kb1) & mb1) << 16);
-          }
-#pragma unroll
-          for (int k = 0; k < kRowsPerBatch; ++k) {
-            if (base + k >= nbr) break;
-            const int pos = past + i_lo + base + k;
-            const int vlo = p.window >= 0 ? pos - p.window : 0;              // first visible key
-            const int vhi = p.causal ? min(total, pos + 1) : total;          // one past the last
-            float2* dst = reinterpret_cast<float2*>(&sm.bias[st][base + k][0]);
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a[k]));
-            const float2 fc = __half22float2(*reinterpret_cast<const __half2*>(&c[k]));
-            dst[lane] = make_float2(ja >= vlo && ja < vhi ? fa.x * kLog2e : -INFINITY,
-                                    ja + 1 >= vlo && ja + 1 < vhi ? fa.y * kLog2e : -INFINITY);
-            dst[32 + lane] = make_float2(jb >= vlo && jb < vhi ? fc.x * kLog2e : -INFINITY,
-                                         jb + 1 >= vlo && jb + 1 < vhi ? fc.y * kLog2e : -INFINITY);
-          }
+        if (elect_one()) {
+          mbar_arrive_tx(&sm.bias_full[st], kBiasBytes);
+          tma_load_2d(&sm.bias[st][0][0], &tmb, kmin + t * kBN, brow0, &sm.bias_full[st]);
         }
-        mbar_arrive(&sm.bias_full[st]);
-        // Pull the next tile's bias lines into L1 so that its loads are short:
-        // 128-byte lines covering keys j0+128 .. j0+255 of every row (addresses
-        // clamped into the row).
-        if (t + 1 < ntiles) {
-          for (int x = lane; x < nbr * 3; x += 32) {
-            const int rho = x / 3, ln = x - rho * 3;
-            const int col = min(j0 + kBN + ln * 64, T - 1);
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(bias0 + (long long)rho * T + col));
-          }
-        }
+        __syncwarp();
+        issued_b = t + 1;
       }
     }
     // Drain: no copy of this CTA may still be landing when it exits.
     mbar_wait(&sm.q_full, 0);
+    for (int t = max(0, issued_b - kNS); t < issued_b; ++t)
+      mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u);
     for (int t = max(0, issued - kNS); t < issued; ++t) {
       mbar_wait(&sm.k_full[t % kNS], (uint32_t)(t / kNS) & 1u);
       mbar_wait(&sm.v_full[t % kNS], (uint32_t)(t / kNS) & 1u);
@@ -592,7 +551,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
                 }
               }
               if constexpr (STAGED) {
-                // Staged bias: fp32, already times log2(e), -inf on masked keys.
+                // Staged bias: fp32, already times log2(e).
                 const float4* b4 = reinterpret_cast<const float4*>(&sm.bias[t % kNS][brow][hf * 64 + c + c16]);
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4) {
@@ -610,7 +569,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
               for (int e = 0; e < 16; ++e) r[c + c16 + e] = __float_as_uint(x[e]);
             }
           }
-          if (!STAGED && !full) {   // warp-uniform: only tiles on a mask boundary pay for the selects
+          if (!full) {   // warp-uniform: only tiles on a mask boundary pay for the selects
 #pragma unroll
             for (int e = 0; e < 64; ++e) {
               const int col = hf * 64 + e;
@@ -727,6 +686,12 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 
 }  // namespace
 
+// A bias shared by all heads is staged by TMA when a CTA's 256 rows span at
+// most kBiasRows query positions (255 / G + 2 bounds the span).
+bool prefill_tc_bias_staged(const Params& p) {
+  return p.has_bias && p.bias_ndim == 1 && 255 / p.G + 2 <= kBiasRows;
+}
+
 bool prefill_tc_supported(const Params& p) {
   // With kv_separate attention reads the new rows in T (fp16 here).
   return p.t_type == kF16 && (p.cache_type == kF16 || p.kv_separate) && p.H == kHD;
@@ -741,7 +706,12 @@ cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps) {
   const void* vsrc = p.kv_separate ? p.kv_sep_v : p.present_v;
   if ((e = encode_fp16_2d_sw128(&maps->m[1], ksrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
     return e;
-  return encode_fp16_2d_sw128(&maps->m[2], vsrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN);
+  if ((e = encode_fp16_2d_sw128(&maps->m[2], vsrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
+    return e;
+  maps->m[3] = maps->m[2];   // a valid map in the bias slot when nothing is staged (never read)
+  if (!prefill_tc_bias_staged(p)) return cudaSuccess;
+  return encode_f32_2d(&maps->m[3], p.bias_stage, (uint64_t)p.bias_bdim * p.S, (uint64_t)p.bias_ld,
+                       (uint64_t)p.bias_stage_ld * 4, kBN, kBiasRows);
 }
 
 namespace {
@@ -753,10 +723,8 @@ bool g_smem_set[5][kMaxDevices];
 cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& maps) {
   const int smem = (int)sizeof(TcSmem) + 1024;
   // The plain kernel scales the row max once, which needs a positive scale.
-  // A bias shared by all heads is staged when a CTA's 256 rows span at most
-  // kBiasRows query positions (255 / G + 2 bounds the span).
   const bool plain = p.softcap <= 0.f && !p.has_bias && p.scale > 0.f;
-  const bool staged = p.has_bias && p.bias_ndim == 1 && 255 / p.G + 2 <= kBiasRows;
+  const bool staged = prefill_tc_bias_staged(p);
   const int mode = plain ? kPlain : staged ? kStagedBias : kGeneric;
   const bool cap = p.softcap > 0.f;
   auto kern = mode == kPlain ? prefill_tc_kernel<kPlain, false>
@@ -773,7 +741,7 @@ cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& m
   }
   const int nrows = p.S * p.G;
   dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
-  kern<<<grid, threads_for(mode), smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2]);
+  kern<<<grid, threads_for(mode), smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2], maps.m[3]);
   return cudaGetLastError();
 }
 

@@ -397,7 +397,29 @@ __global__ void __launch_bounds__(kShiftThreads) window_shift_kernel(const Param
   }
 }
 
+// Bias staging for the tensor-core prefill: bias[bb, 0, i, j] * log2(e) as fp32
+// rows of bias_stage_ld floats (16-byte stride), so that the prefill's TMA warp
+// loads a (positions x 128 keys) block with one tensor copy.
+__global__ void __launch_bounds__(256) bias_stage_kernel(const Params p) {
+  const long long rows = (long long)p.bias_bdim * p.S;
+  const int T = p.bias_ld;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < rows * T;
+       x += (long long)gridDim.x * blockDim.x) {
+    const long long r = x / T;
+    const int j = (int)(x - r * T);
+    p.bias_stage[r * p.bias_stage_ld + j] = load_t(p.bias, x, p.t_type) * kLog2e;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bias_stage(const Params& p, cudaStream_t st) {
+  const long long n = (long long)p.bias_bdim * p.S * p.bias_ld;
+  const unsigned blocks = (unsigned)min((n + 255) / 256, 152LL * 16);
+  if (blocks == 0) return cudaSuccess;
+  bias_stage_kernel<<<blocks, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_window_shift(const Params& p, cudaStream_t st) {
   const int esize = p.cache_type == kF32 ? 4 : (p.cache_type == kF16 ? 2 : 1);

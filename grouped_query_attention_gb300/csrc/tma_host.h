@@ -19,4 +19,10 @@ cudaError_t encode_fp16_2d_sw128(CUtensorMap* map, const void* base, uint64_t ro
 cudaError_t encode_u8_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                                uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
 
+// 2D map of a row-major [rows][cols] fp32 matrix without swizzle: boxes of
+// box_cols (<= 256) x box_rows elements land as box_rows rows of box_cols
+// consecutive floats; elements past the matrix are read as zero.
+cudaError_t encode_f32_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                          uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
+
 }  // namespace gqa

@@ -253,6 +253,7 @@ GQA_API gqa_status gqa_describe_plan(const gqa_handle* handle, const gqa_inputs*
 #define GQA_KERNEL_PREFILL_TENSOR_CORE 5
 #define GQA_KERNEL_DECODE_TENSOR_CORE 6
 #define GQA_KERNEL_WINDOW_SHIFT 7
+#define GQA_KERNEL_BIAS_STAGE 8
 GQA_API gqa_status gqa_profile_begin(gqa_handle* handle, int32_t max_launches);
 GQA_API gqa_status gqa_profile_end(gqa_handle* handle, int32_t* kinds, float* ms, int32_t capacity, int32_t* count);
 
