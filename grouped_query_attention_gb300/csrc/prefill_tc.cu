@@ -101,7 +101,6 @@ struct ScoreConst {
   float k_add;    // c log2(e)
   float k_u;      // scale / c
   float k_w;      // scale * log2(e)
-  float raw_poly; // largest |raw| with |u| <= 1/2
 };
 
 __device__ __forceinline__ ScoreConst score_const(const Params& p) {
@@ -111,7 +110,6 @@ __device__ __forceinline__ ScoreConst score_const(const Params& p) {
   k.k_add = p.softcap * kLog2e;
   k.k_u = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
   k.k_w = p.scale * kLog2e;
-  k.raw_poly = 0.5f / fabsf(k.k_u);
   return k;
 }
 
@@ -125,11 +123,12 @@ constexpr float kTanhP3 = -5.389288813e-02f;
 constexpr float kTanhP4 = 2.127229236e-02f;
 constexpr float kTanhP5 = -6.609579083e-03f;
 
-// Softcapped score of two raw products on the FMA pipe (|u| <= 1/2), log2 domain.
-__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k) {
+// Softcapped score of two raw products on the FMA pipe (valid for |u| <= 1/2;
+// z = u^2 is returned for the check), log2 domain.
+__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k, float2& z) {
   const float2 zero = make_float2(0.f, 0.f);
   const float2 u = ffma2(raw, make_float2(k.k_u, k.k_u), zero);
-  const float2 z = ffma2(u, u, zero);
+  z = ffma2(u, u, zero);
   float2 q = ffma2(z, make_float2(kTanhP5, kTanhP5), make_float2(kTanhP4, kTanhP4));
   q = ffma2(q, z, make_float2(kTanhP3, kTanhP3));
   q = ffma2(q, z, make_float2(kTanhP2, kTanhP2));
@@ -519,55 +518,69 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           tmem_ld32(s_addr + hf * 64, r);
           tmem_ld32(s_addr + hf * 64 + 32, r + 32);
           tmem_ld_wait();
-          bool poly = false;   // softcap on the FMA pipe for this half (warp-uniform)
-          if constexpr (CAP) {
-            float am[4] = {0.f, 0.f, 0.f, 0.f};   // four independent chains
+          // Transform the half in place: scale, softcap, bias. With a softcap the
+          // FMA-pipe polynomial goes first and is checked afterwards (|u| <= 1/2
+          // on every lane of the warp, from the largest u^2); otherwise the raw
+          // scores are read again from tensor memory (intact: P of this half is
+          // written after it) and take the exp2 / reciprocal form.
+          auto transform = [&](bool poly) -> float {
+            float zmax = 0.f;
 #pragma unroll
-            for (int e = 0; e < 64; e += 2)
-              am[(e >> 1) & 3] = fmax3(am[(e >> 1) & 3], fabsf(__uint_as_float(r[e])), fabsf(__uint_as_float(r[e + 1])));
-            poly = __all_sync(0xffffffffu, fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3])) <= kc.raw_poly);
-          }
+            for (int c = 0; c < 64; c += 32) {
+              float bv[32];
+              if constexpr (!STAGED) load_bias32(bias_row, j0 + hf * 64 + c, hf * 64 + c, lo, hi, bv);
 #pragma unroll
-          for (int c = 0; c < 64; c += 32) {
-            float bv[32];
-            if constexpr (!STAGED) load_bias32(bias_row, j0 + hf * 64 + c, hf * 64 + c, lo, hi, bv);
+              for (int c16 = 0; c16 < 32; c16 += 16) {   // 16 independent chains at a time
+                float x[16];
+                if (CAP && poly) {
 #pragma unroll
-            for (int c16 = 0; c16 < 32; c16 += 16) {   // 16 independent chains at a time
-              float x[16];
-              if (CAP && poly) {
+                  for (int e = 0; e < 16; e += 2) {
+                    float2 z;
+                    const float2 y = softcap_poly2(
+                        make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1])), kc, z);
+                    x[e] = y.x;
+                    x[e + 1] = y.y;
+                    zmax = fmax3(zmax, z.x, z.y);
+                  }
+                } else {
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                  const float2 y = softcap_poly2(
-                      make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1])), kc);
-                  x[e] = y.x;
-                  x[e + 1] = y.y;
+                  for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[c + c16 + e]) * kc.k_raw;
+                  if constexpr (CAP) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] = fmaf(rcp_approx(ex2(x[e]) + 1.0f), kc.k_mul, kc.k_add);
+                  }
                 }
-              } else {
+                if constexpr (STAGED) {
+                  // Staged bias: fp32, already times log2(e).
+                  const float4* b4 = reinterpret_cast<const float4*>(&sm.bias[t % kNS][brow][hf * 64 + c + c16]);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[c + c16 + e]) * kc.k_raw;
-                if constexpr (CAP) {
+                  for (int e4 = 0; e4 < 4; ++e4) {
+                    const float4 bq = b4[e4];
+                    x[4 * e4] += bq.x;
+                    x[4 * e4 + 1] += bq.y;
+                    x[4 * e4 + 2] += bq.z;
+                    x[4 * e4 + 3] += bq.w;
+                  }
+                } else {
 #pragma unroll
-                  for (int e = 0; e < 16; ++e) x[e] = fmaf(rcp_approx(ex2(x[e]) + 1.0f), kc.k_mul, kc.k_add);
+                  for (int e = 0; e < 16; ++e) x[e] = fmaf(bv[c16 + e], kLog2e, x[e]);
                 }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[c + c16 + e] = __float_as_uint(x[e]);
               }
-              if constexpr (STAGED) {
-                // Staged bias: fp32, already times log2(e).
-                const float4* b4 = reinterpret_cast<const float4*>(&sm.bias[t % kNS][brow][hf * 64 + c + c16]);
-#pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                  const float4 bq = b4[e4];
-                  x[4 * e4] += bq.x;
-                  x[4 * e4 + 1] += bq.y;
-                  x[4 * e4 + 2] += bq.z;
-                  x[4 * e4 + 3] += bq.w;
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) x[e] = fmaf(bv[c16 + e], kLog2e, x[e]);
-              }
-#pragma unroll
-              for (int e = 0; e < 16; ++e) r[c + c16 + e] = __float_as_uint(x[e]);
             }
+            return zmax;
+          };
+          if constexpr (CAP) {
+            const float zmax = transform(true);
+            if (__any_sync(0xffffffffu, !(zmax <= 0.25f))) {
+              tmem_ld32(s_addr + hf * 64, r);
+              tmem_ld32(s_addr + hf * 64 + 32, r + 32);
+              tmem_ld_wait();
+              transform(false);
+            }
+          } else {
+            transform(false);
           }
           if (!full) {   // warp-uniform: only tiles on a mask boundary pay for the selects
 #pragma unroll
