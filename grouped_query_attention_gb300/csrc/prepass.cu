@@ -399,22 +399,27 @@ __global__ void __launch_bounds__(kShiftThreads) window_shift_kernel(const Param
 
 // Bias staging for the tensor-core prefill: bias[bb, 0, i, j] * log2(e) as fp32
 // rows of bias_stage_ld floats (16-byte stride), so that the prefill's TMA warp
-// loads a (positions x 128 keys) block with one tensor copy.
+// loads a (positions x 128 keys) block with one tensor copy. A thread converts
+// four consecutive keys of a row (one 16-byte store; the row's tail past T is
+// never read by the copies, which stop at T).
 __global__ void __launch_bounds__(256) bias_stage_kernel(const Params p) {
   const long long rows = (long long)p.bias_bdim * p.S;
-  const int T = p.bias_ld;
-  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < rows * T;
+  const int T = p.bias_ld, q4 = (T + 3) / 4;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < rows * q4;
        x += (long long)gridDim.x * blockDim.x) {
-    const long long r = x / T;
-    const int j = (int)(x - r * T);
-    p.bias_stage[r * p.bias_stage_ld + j] = load_t(p.bias, x, p.t_type) * kLog2e;
+    const long long r = x / q4;
+    const int j = (int)(x - r * q4) * 4;
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = j + k < T ? load_t(p.bias, r * T + j + k, p.t_type) * kLog2e : 0.f;
+    *reinterpret_cast<float4*>(p.bias_stage + r * p.bias_stage_ld + j) = make_float4(v[0], v[1], v[2], v[3]);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_bias_stage(const Params& p, cudaStream_t st) {
-  const long long n = (long long)p.bias_bdim * p.S * p.bias_ld;
+  const long long n = (long long)p.bias_bdim * p.S * ((p.bias_ld + 3) / 4);
   const unsigned blocks = (unsigned)min((n + 255) / 256, 152LL * 16);
   if (blocks == 0) return cudaSuccess;
   bias_stage_kernel<<<blocks, 256, 0, st>>>(p);
