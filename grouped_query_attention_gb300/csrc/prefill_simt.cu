@@ -120,15 +120,14 @@ prefill_simt_kernel(const Params p) {
     pos_r[i] = past_row + i_r[i];          // position in cache rows
   }
   const float qscale = p.softcap > 0.f ? p.scale : p.scale * kLog2e;
-  float m[4], l[4], o[4][NC][4];
+  float m[4], l[4];
+  float2 o2[4][NC][2];   // rows x chunks x dim pairs
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     m[i] = kNegBig;
     l[i] = 0.f;
 #pragma unroll
-    for (int c = 0; c < NC; ++c)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[i][c][e] = 0.f;
+    for (int c = 0; c < NC; ++c) o2[i][c][0] = o2[i][c][1] = make_float2(0.f, 0.f);
   }
 
   // Attention reads the present cache, or the new rows in T when a prompt's
@@ -165,21 +164,31 @@ prefill_simt_kernel(const Params p) {
     }
     __syncthreads();
 
-    // Scores of rows 4rg.. x keys 4kg.. : one 16-byte load of Q^T and of K^T per coordinate.
-    float s[4][4];
+    // Scores of rows 4rg.. x keys 4kg.. : one 16-byte load of Q^T and of K^T per
+    // coordinate, 16 FMAs as 8 packed fp32x2 ones (key pairs).
+    float2 s2[4][2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+    for (int i = 0; i < 4; ++i) s2[i][0] = s2[i][1] = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int d = 0; d < H; ++d) {
       const float4 qv = *reinterpret_cast<const float4*>(&qT[d * kR + 4 * rg]);
       const float4 kv = *reinterpret_cast<const float4*>(&kT[d * kKP + 4 * kg]);
-      const float qa[4] = {qv.x, qv.y, qv.z, qv.w}, ka[4] = {kv.x, kv.y, kv.z, kv.w};
+      const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+      const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i) {
+        const float2 qq = make_float2(qa[i], qa[i]);
+        s2[i][0] = ffma2(qq, k01, s2[i][0]);
+        s2[i][1] = ffma2(qq, k23, s2[i][1]);
+      }
+    }
+    float s[4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[i][j] = fmaf(qa[i], ka[j], s[i][j]);
+    for (int i = 0; i < 4; ++i) {
+      s[i][0] = s2[i][0].x;
+      s[i][1] = s2[i][0].y;
+      s[i][2] = s2[i][1].x;
+      s[i][3] = s2[i][1].y;
     }
     // Scale, softcap, bias (log2 domain), masks: causal / window in cache rows,
     // bias columns at absolute positions.
@@ -219,10 +228,12 @@ prefill_simt_kernel(const Params p) {
 #pragma unroll
       for (int o16 = 8; o16 > 0; o16 >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o16, 16);
       l[i] = l[i] * f + sum;
+      const float2 f2 = make_float2(f, f), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < NC; ++c)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[i][c][e] *= f;
+      for (int c = 0; c < NC; ++c) {
+        o2[i][c][0] = ffma2(o2[i][c][0], f2, z2);
+        o2[i][c][1] = ffma2(o2[i][c][1], f2, z2);
+      }
       *reinterpret_cast<float4*>(&ps[(4 * rg + i) * kKP + 4 * kg]) = make_float4(s[i][0], s[i][1], s[i][2], s[i][3]);
     }
     __syncthreads();
@@ -245,12 +256,12 @@ prefill_simt_kernel(const Params p) {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
           const float4 vv = *reinterpret_cast<const float4*>(&vs[(j4 + k) * HMAX + 64 * c + 4 * kg]);
+          const float2 v01 = make_float2(vv.x, vv.y), v23 = make_float2(vv.z, vv.w);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            o[i][c][0] = fmaf(pr[i][k], vv.x, o[i][c][0]);
-            o[i][c][1] = fmaf(pr[i][k], vv.y, o[i][c][1]);
-            o[i][c][2] = fmaf(pr[i][k], vv.z, o[i][c][2]);
-            o[i][c][3] = fmaf(pr[i][k], vv.w, o[i][c][3]);
+          for (int i = 0; i < 4; ++i) {   // packed fp32x2 FMAs over dim pairs
+            const float2 pp = make_float2(pr[i][k], pr[i][k]);
+            o2[i][c][0] = ffma2(pp, v01, o2[i][c][0]);
+            o2[i][c][1] = ffma2(pp, v23, o2[i][c][1]);
           }
         }
       }
@@ -277,7 +288,7 @@ prefill_simt_kernel(const Params p) {
     for (int c = 0; c < NC; ++c) {
       const int d = 64 * c + 4 * kg;
       if (d >= H) continue;
-      const float4 v = make_float4(o[i][c][0] * sc, o[i][c][1] * sc, o[i][c][2] * sc, o[i][c][3] * sc);
+      const float4 v = make_float4(o2[i][c][0].x * sc, o2[i][c][0].y * sc, o2[i][c][1].x * sc, o2[i][c][1].y * sc);
       if constexpr (sizeof(T) == 2) {
         uint2 u;
         *reinterpret_cast<__half2*>(&u.x) = __floats2half2_rn(v.x, v.y);

@@ -87,6 +87,11 @@ PREFILL = {
     "f32_chunk_all_features": spec(dtype="f32", S=9, N=8, Nkv=2, local_window_size=50, softcap=20.0,
                                    bias=(3, 8, 0.5), head_sink=True, qk_norm=True, rotary_theta=1e4),
     "i8_per_channel_prefill": spec(dtype="f32", S=17, quant="PER_CHANNEL"),
+    "i8_per_tensor_prefill_all_features": spec(dtype="f32", S=40, N=8, Nkv=2, quant="PER_TENSOR",
+                                               scale_range=(0.02, 0.04), local_window_size=60, softcap=20.0,
+                                               bias=(3, 8, 0.5), head_sink=True, qk_norm=True, rotary_theta=1e4),
+    "i8_per_channel_prompt_h64_g8": spec(dtype="f32", H=64, N=16, Nkv=2, S=70, mode="prompt", capacity=80,
+                                         seqlens_k=(69, 33, 1), seqlens_range=None, quant="PER_CHANNEL"),
     "f16_h256_g2": spec(H=256, N=4, Nkv=2, S=20, capacity=500, seqlens_range=(20, 480)),
     "f16_h128_g8_s65": spec(N=16, Nkv=2, S=65, seqlens_range=(65, 700), rotary_theta=1e4, qk_norm=True),
     "f16_copy_s12": spec(S=12, N=8, Nkv=2, mode="copy", past_len=300, seqlens_range=(11, 311)),
