@@ -38,6 +38,10 @@ DECODE = {
                                   rotary_theta=1e4),
     "f32_g1_bias_shared": spec(dtype="f32", N=2, Nkv=2, bias=(1, 1, 0.5), seqlens_range=(0, 300)),
     "f16_long_many_splits": spec(B=2, capacity=6000, seqlens_range=(3000, 5999)),
+    # degenerate windows and groups: a window of 0 keys besides self, one KV head for 64 query heads
+    "f16_window0_decode": spec(local_window_size=0, rotary_theta=1e4),
+    "f32_window1_g1_decode": spec(dtype="f32", N=2, Nkv=2, local_window_size=1, seqlens_range=(0, 300)),
+    "f16_g64_decode_shape_prefill": spec(N=64, Nkv=1, seqlens_range=(100, 700), rotary_theta=1e4),
     # sliding-window cache: rows evicted from the front, compacted in place, new rows appended
     "f16_window_cache_decode": spec(S=1, capacity=300, seqlens_range=(250, 900), local_window_size=200,
                                     sliding_window_cache=1, rotary_theta=1e4),
@@ -107,6 +111,9 @@ PREFILL = {
                                  seqlens_k=(129, 100, 7), seqlens_range=None),
     "f16_tc_smooth_multi_block": spec(B=2, S=300, N=8, Nkv=2, capacity=2500, seqlens_range=(300, 2400),
                                       smooth_softmax=1, rotary_theta=1e4),
+    "f16_tc_window0": spec(S=40, N=16, Nkv=2, local_window_size=0, seqlens_range=(40, 700)),
+    "f16_tc_single_key_prompt": spec(S=1, N=8, Nkv=1, mode="prompt", capacity=1, seqlens_k=(0, 0, 0),
+                                     seqlens_range=None, rotary_theta=1e4, qk_norm=True),
     # bias shared by all heads with G >= 8: staged through shared memory by the TMA warp
     "f16_tc_staged_bias_softcap_window": spec(S=70, N=16, Nkv=2, local_window_size=90, softcap=30.0,
                                               bias=(3, 1, 0.5), head_sink=True, rotary_theta=1e4,
