@@ -123,9 +123,10 @@ constexpr float kTanhP3 = -5.389288813e-02f;
 constexpr float kTanhP4 = 2.127229236e-02f;
 constexpr float kTanhP5 = -6.609579083e-03f;
 
-// Softcapped score of two raw products on the FMA pipe (valid for |u| <= 1/2;
+// Softcapped score of two raw products on the FMA pipe plus `add` (the bias
+// in the log2 domain) in the last fused multiply-add (valid for |u| <= 1/2;
 // z = u^2 is returned for the check), log2 domain.
-__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k, float2& z) {
+__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k, float2& z, float2 add) {
   const float2 zero = make_float2(0.f, 0.f);
   const float2 u = ffma2(raw, make_float2(k.k_u, k.k_u), zero);
   z = ffma2(u, u, zero);
@@ -135,7 +136,7 @@ __device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k,
   q = ffma2(q, z, make_float2(kTanhP1, kTanhP1));
   q = ffma2(q, z, make_float2(1.f, 1.f));
   const float2 w = ffma2(raw, make_float2(k.k_w, k.k_w), zero);
-  return ffma2(w, q, zero);
+  return ffma2(w, q, add);
 }
 
 
@@ -532,16 +533,33 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 #pragma unroll
               for (int c16 = 0; c16 < 32; c16 += 16) {   // 16 independent chains at a time
                 float x[16];
-                if (CAP && poly) {
+                if (CAP && poly) {   // bias added in the polynomial's last fused multiply-add
+                  float ba[16];
+                  if constexpr (STAGED) {
+                    const float4* b4 = reinterpret_cast<const float4*>(&sm.bias[t % kNS][brow][hf * 64 + c + c16]);
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                      const float4 bq = b4[e4];
+                      ba[4 * e4] = bq.x;
+                      ba[4 * e4 + 1] = bq.y;
+                      ba[4 * e4 + 2] = bq.z;
+                      ba[4 * e4 + 3] = bq.w;
+                    }
+                  } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ba[e] = bv[c16 + e] * kLog2e;
+                  }
 #pragma unroll
                   for (int e = 0; e < 16; e += 2) {
                     float2 z;
                     const float2 y = softcap_poly2(
-                        make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1])), kc, z);
-                    x[e] = y.x;
-                    x[e + 1] = y.y;
+                        make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1])), kc, z,
+                        make_float2(ba[e], ba[e + 1]));
+                    r[c + c16 + e] = __float_as_uint(y.x);
+                    r[c + c16 + e + 1] = __float_as_uint(y.y);
                     zmax = fmax3(zmax, z.x, z.y);
                   }
+                  continue;   // scores and bias done for this group
                 } else {
 #pragma unroll
                   for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r[c + c16 + e]) * kc.k_raw;
