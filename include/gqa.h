@@ -6,7 +6,9 @@
  * grouped-query attention over BSH query/key/value and a BNSH key/value cache,
  * with optional paired Q/K RMS normalisation, NeoX rotary embedding, causal
  * and local-window masks, additive attention bias, softcap, head sink /
- * smooth softmax and an int8 (per-tensor or per-channel) quantised cache.
+ * smooth softmax, an int8 (per-tensor or per-channel) or, for prompts, a
+ * packed 4-bit quantised cache, a sliding-window (window-shift) cache, and a
+ * prompt's float cache in the other float dtype.
  *
  * Conventions for every entry point:
  *   - All tensors are dense, row-major (C-contiguous) and live in device

@@ -289,3 +289,22 @@ def test_misaligned_pointer_rejected():
     c = FakeCall()
     c.inp.query.data = c.inp.query.data + 2
     _expect(c, capi.GQA_ERR_INVALID_ARGUMENT)
+
+
+def test_c_abi_from_plain_c(tmp_path):
+    """include/gqa.h compiles as C11 and the library links and answers host-only calls from C."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(capi.LIB_PATH)
+    exe = str(tmp_path / "host_check")
+    cmd = [gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c_abi", "host_check.c"), "-L", libdir, "-lgqa_gb300",
+           "-Wl,-rpath," + libdir, "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert "c abi host check: ok" in r.stdout
