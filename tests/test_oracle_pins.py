@@ -597,3 +597,62 @@ def test_rejects_inconsistent_inputs():
     with pytest.raises(ValueError):
         oracle.gqa_forward(case["inputs"], dict(case["attrs"], num_heads=3), case["present_key"],
                            case["present_value"])
+
+
+# ---------------------------------------------------------------- randomized sweep against the brute force
+
+def _random_spec(rng):
+    Nkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([1, 2, 3]))
+    H = int(rng.choice([4, 8]))
+    dtype = str(rng.choice(["f32", "f16"]))
+    mode = str(rng.choice(["prompt", "shared", "copy"]))
+    S = int(rng.integers(1, 4))
+    B = int(rng.integers(1, 3))
+    kw = dict(name="r", dtype=dtype, B=B, S=S, N=G * Nkv, Nkv=Nkv, H=H, mode=mode)
+    if mode == "prompt":
+        kw.update(capacity=S + int(rng.integers(0, 2)), seqlens_k=tuple(int(x) for x in rng.integers(0, S, B)))
+    elif mode == "shared":
+        cap = S + int(rng.integers(1, 5))
+        kw.update(capacity=cap, seqlens_k=tuple(int(x) for x in rng.integers(S - 1, cap, B)))
+    else:
+        past = int(rng.integers(1, 5))
+        kw.update(capacity=past + S, past_len=past, seqlens_k=tuple(int(x) for x in rng.integers(S - 1, past + S, B)))
+    causal = int(rng.integers(0, 2)) if mode == "prompt" else 1
+    kw["causal"] = causal
+    if causal and rng.random() < 0.4:
+        kw["local_window_size"] = int(rng.integers(0, 4))
+    if rng.random() < 0.4:
+        kw["rotary_theta"] = 1e4
+    if rng.random() < 0.3:
+        kw["qk_norm"] = True
+    if rng.random() < 0.3:
+        kw["softcap"] = float(rng.choice([0.5, 3.0]))
+    if rng.random() < 0.3:
+        kw["bias"] = (int(rng.choice([1, B])), int(rng.choice([1, G * Nkv])), 0.5)
+    if rng.random() < 0.3:
+        kw["head_sink"] = True
+    elif rng.random() < 0.3:
+        kw["smooth_softmax"] = 1
+    if dtype == "f32" and mode != "copy" and rng.random() < 0.3:
+        kw.update(quant=str(rng.choice(["PER_TENSOR", "PER_CHANNEL"])), scale_range=(0.02, 0.2))
+        if mode == "prompt" and rng.random() < 0.5:
+            kw["bits"] = 4
+    return CaseSpec(**kw)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_configs_match_brute_force(seed):
+    """Random small configurations (modes, features, quantised caches, dtypes) against the
+    independently written brute force: outputs to 1e-11 relative, caches exactly."""
+    spec = _random_spec(np.random.default_rng(1000 + seed))
+    case = generate(spec, seed=seed)
+    res = run(case)
+    out_b, pk_b, pv_b = brute_forward(case["inputs"], case["attrs"], case["present_key"], case["present_value"],
+                                      case["share_buffer"])
+    np.testing.assert_allclose(res["output_f64"], out_b, rtol=1e-11, atol=1e-12)
+    for got, want in ((res["present_key"], pk_b), (res["present_value"], pv_b)):
+        if got.dtype in (np.int8, np.uint8):
+            assert np.array_equal(got, want)
+        else:
+            np.testing.assert_allclose(got.astype(np.float64), want.astype(np.float64), rtol=2e-7, atol=0)
