@@ -308,3 +308,22 @@ def test_c_abi_from_plain_c(tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert "c abi host check: ok" in r.stdout
+
+
+def test_bias_staging_plan():
+    """A bias shared by all heads with G >= 8 on the tensor-core prefill adds the bias-staging
+    launch and its workspace (rows of a 16-byte multiple); per-head bias or G < 8 does not."""
+    def plan(N, ndim, T=130):
+        c = FakeCall(S=64, C=256, N=N, Nkv=2)
+        c.inp.total_sequence_length = T
+        c.inp.attention_bias = c.t(capi.GQA_F16, (1, ndim, 64, T))
+        h = capi.gqa_create(capi.make_attrs(**c.attrs))
+        try:
+            return capi.gqa_describe_plan(h, c.inp, c.out)
+        finally:
+            capi.gqa_destroy(h)
+    staged, per_head, small_group = plan(16, 1), plan(16, 16), plan(8, 1)
+    assert staged.launches == 3 and per_head.launches == 2 and small_group.launches == 2
+    # staged bias: 64 rows x ceil(130 / 4) * 4 floats, 256-byte aligned
+    extra = staged.workspace_bytes - per_head.workspace_bytes
+    assert extra >= 64 * 132 * 4 and extra < 64 * 132 * 4 + 256
