@@ -15,9 +15,12 @@ Pins: every function is checked in ``tests/test_oracle_pins.py`` against
 closed forms, invariants, a pure-Python brute force and a library routine
 (``torch.nn.functional.scaled_dot_product_attention`` in fp64). Readings that
 the pages leave open (query-head to KV-head mapping, window bound, order of
-softcap and bias, int8 rounding) are fixed by explicit switches whose default
-is the documented reading; those readings are "parity unpinned" by the pages
-themselves and are listed as such in the design notes.
+softcap and bias, head-sink placement, int8 rounding, the 4-bit code range,
+the row layout of a sliding-window cache) are fixed by explicit switches or
+single documented choices; those readings are "parity unpinned" by the pages
+themselves and are listed as such in the design notes. The 4-bit nibble
+layout is pinned by the pages' description (+8 bias, even coordinate low) and
+the sliding-window cache by equality with attention over the full history.
 """
 
 from .gqa import (  # noqa: F401
