@@ -327,3 +327,16 @@ def test_bias_staging_plan():
     # staged bias: 64 rows x ceil(130 / 4) * 4 floats, 256-byte aligned
     extra = staged.workspace_bytes - per_head.workspace_bytes
     assert extra >= 64 * 132 * 4 and extra < 64 * 132 * 4 + 256
+
+
+def test_binding_constants_match_header():
+    """The ctypes binding's enum values and kernel kinds are the header's."""
+    header = open(os.path.join(ROOT, "include", "gqa.h")).read()
+    kinds = {int(v): k for k, v in re.findall(r"#define GQA_KERNEL_(\w+) (\d+)", header)}
+    assert {k: v.lower() for k, v in kinds.items()} == {k: v for k, v in capi.KERNEL_KINDS.items()}
+    dt = dict(re.findall(r"(GQA_(?:DTYPE_NONE|F32|F16|I8|U8|I32|BF16)) = (\d+)", header))
+    for name, value in dt.items():
+        assert getattr(capi, name) == int(value), name
+    reg = dict(re.findall(r"#define (GQA_REGIME_\w+) (\d+)", header))
+    for name, value in reg.items():
+        assert getattr(capi, name) == int(value), name
