@@ -13,7 +13,10 @@ Inputs, Outputs, Attributes, Type constraints, Implementation variants).
 
 Pins: every function is checked in ``tests/test_oracle_pins.py`` against
 closed forms, invariants, a pure-Python brute force and a library routine
-(``torch.nn.functional.scaled_dot_product_attention`` in fp64). Readings that
+(``torch.nn.functional.scaled_dot_product_attention`` in fp64). The fp32
+recipe of the stored K rows (``rms_norm_fp32``, ``rotary_neox_fp32``) is
+pinned in ``tests/test_oracle_fp32_recipe.py``: bit for bit against a scalar
+restatement, and within its rounding-error bound of the fp64 definition. Readings that
 the pages leave open (query-head to KV-head mapping, window bound, order of
 softcap and bias, head-sink placement, int8 rounding, the 4-bit code range,
 the row layout of a sliding-window cache) are fixed by explicit switches or
@@ -31,7 +34,9 @@ from .gqa import (  # noqa: F401
     quantize_int4,
     quantize_int8,
     rms_norm,
+    rms_norm_fp32,
     rotary_neox,
+    rotary_neox_fp32,
     softcap_scores,
     unpack_int4,
 )

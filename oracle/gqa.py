@@ -35,6 +35,11 @@ the readings the library implements):
     C >= S + W and L >= W, so every key a query can see is kept. Without a
     past cache the flag changes nothing;
   * RMS norm y = x / sqrt(mean(x^2) + eps) * w, weight used as given;
+  * the K rows stored in the cache are computed in fp32 in one fixed order
+    (rms_norm_fp32, rotary_neox_fp32) and then cast or quantised, so that the
+    stored bytes are reproducible; attention reads those stored values. The
+    fp64 functions define the mathematics and pin the fp32 recipe within its
+    rounding-error bound (the pages fix no evaluation order);
   * padding rows of a prompt (i >= total_b, no past) produce a zero output row;
     their K/V rows are still appended.
 """
@@ -89,6 +94,65 @@ def rotary_neox(x: np.ndarray, cos_row: np.ndarray, sin_row: np.ndarray) -> np.n
     s = np.asarray(sin_row, dtype=np.float64)
     half = x.shape[-1] // 2
     x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def _sum_squares_fp32(x32: np.ndarray) -> np.ndarray:
+    """Sum of squares over the last axis in the fp32 order of the stored-row recipe.
+
+    Every square is rounded to fp32; the squares of each group of four
+    consecutive coordinates are added left to right; the H/4 group sums are
+    then added as a pairwise tree (neighbours first: (g0+g1), (g2+g3), ...,
+    then the pairs of pairs, ...), the group sums padded with zeros to a power
+    of two. Each addition is one fp32 rounding.
+    """
+    sq = x32 * x32
+    g = sq[..., 0::4]
+    for k in (1, 2, 3):
+        g = g + sq[..., k::4]
+    n = g.shape[-1]
+    width = 1
+    while width < n:
+        width *= 2
+    if width > n:
+        g = np.concatenate([g, np.zeros(g.shape[:-1] + (width - n,), np.float32)], axis=-1)
+    while g.shape[-1] > 1:
+        g = g[..., 0::2] + g[..., 1::2]
+    return g[..., 0]
+
+
+def rms_norm_fp32(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """RMS normalisation of the rows that are stored in the cache, in fp32.
+
+    Same function as rms_norm (section Inputs, q_norm_weight / k_norm_weight;
+    section Attributes, qk_norm_epsilon), evaluated in one fixed fp32 order so
+    that the stored bytes are reproducible: ss = _sum_squares_fp32(x);
+    ms = ss / H; r = 1 / sqrt(ms + eps) (IEEE division and square root, each
+    rounded); y = (x * r) * w as two rounded products. The pages fix no
+    evaluation order; this one (groups of four coordinates, then a pairwise
+    tree) is the reading the library follows.
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    w32 = np.asarray(weight, dtype=np.float32)
+    H = x32.shape[-1]
+    ms = _sum_squares_fp32(x32) / np.float32(H)
+    r = np.float32(1.0) / np.sqrt(ms + np.float32(eps))
+    return (x32 * r[..., None]) * w32
+
+
+def rotary_neox_fp32(x: np.ndarray, cos_row: np.ndarray, sin_row: np.ndarray) -> np.ndarray:
+    """NeoX rotary of stored rows in fp32: every product rounded, then one add or subtract.
+
+    Same function as rotary_neox (section Inputs, cos_cache / sin_cache) in a
+    fixed fp32 order: y[d] = fl(x[d] c) - fl(x[d+H/2] s) and y[d+H/2] =
+    fl(x[d+H/2] c) + fl(x[d] s), each result rounded once (no fused
+    multiply-add), with c, s the table entries converted exactly to fp32.
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    c = np.asarray(cos_row, dtype=np.float32)
+    s = np.asarray(sin_row, dtype=np.float32)
+    half = x32.shape[-1] // 2
+    x1, x2 = x32[..., :half], x32[..., half:]
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
@@ -212,8 +276,9 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
       are always updated in full.
     Returns output (dtype of query), output_f64, present_key/value, and the
     fp64 values of the appended rows before the storage cast
-    (appended_key_f64 / appended_value_f64, (B, N_kv, S, H)) with their
-    cache rows (appended_pos, (B, S)).
+    (appended_key_f64 / appended_value_f64, (B, N_kv, S, H); the stored K
+    rows come from the fp32 recipe instead) with their cache rows
+    (appended_pos, (B, S)).
 
     com.microsoft.GroupQueryAttention: section Description (grouped-query
     attention over BSH Q/K/V and BNSH caches), sections Inputs / Outputs /
@@ -330,14 +395,19 @@ def gqa_forward(inputs: dict, attrs: dict, present_key: np.ndarray | None = None
         for g in range(Nkv):
             kr = k_in[b, :, g * H:(g + 1) * H].astype(np.float64)
             vr = v_in[b, :, g * H:(g + 1) * H].astype(np.float64)
+            # The stored K row is the fp32 recipe (rms_norm_fp32, rotary_neox_fp32);
+            # the fp64 row is kept beside it for the cross-check of that recipe.
+            k32 = k_in[b, :, g * H:(g + 1) * H].astype(np.float32)
             if kw is not None:
                 kr = rms_norm(kr, kw, eps)
+                k32 = rms_norm_fp32(k32, kw, eps)
             if rotary:
                 kr = rotary_neox(kr, cos_c[pos], sin_c[pos])
-            pk[b, g, rows_new] = _store(kr, pk.dtype, kq, k_scale, g, H, bits)
+                k32 = rotary_neox_fp32(k32, inputs["cos_cache"][pos], inputs["sin_cache"][pos])
+            pk[b, g, rows_new] = _store(k32, pk.dtype, kq, k_scale, g, H, bits)
             pv[b, g, rows_new] = _store(vr, pv.dtype, vq, v_scale, g, H, bits)
             if separate:   # the rows attention reads: the query dtype
-                attn_k[b, g, rows_new] = kr.astype(out_dtype)
+                attn_k[b, g, rows_new] = k32.astype(out_dtype)
                 attn_v[b, g, rows_new] = vr.astype(out_dtype)
             new_k[b, g], new_v[b, g] = kr, vr
         new_pos[b] = rows_new

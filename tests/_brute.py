@@ -1,10 +1,11 @@
 """Pure-Python scalar brute force of the GroupQueryAttention forward pass.
 
 A second, independently written formulation used only to pin the numpy
-oracle on tiny shapes: scalar loops over every index, rotary as a complex
-multiplication, RMS norm and every sum through ``math.fsum``, the softmax as
-exp(s - logsumexp) with the sink logit inside the log-sum-exp. It shares no
-code with ``oracle/``.
+oracle on tiny shapes: scalar loops over every index, rotary of queries as a
+complex multiplication, their RMS norm and every sum through ``math.fsum``,
+the softmax as exp(s - logsumexp) with the sink logit inside the log-sum-exp;
+stored K rows through a scalar fp32 restatement of the stored-row recipe
+(recursive pairwise tree). It shares no code with ``oracle/``.
 """
 
 import math
@@ -14,6 +15,51 @@ import numpy as np
 
 def _f(x):
     return float(x)
+
+
+# Stored K rows follow the fp32 recipe: every operation rounded to fp32 (a
+# double result of two fp32 operands rounds to the correctly rounded fp32
+# result for +, -, *, / and sqrt), squares summed left to right in groups of
+# four, the group sums added as a balanced binary tree (recursive halving of
+# the group list padded with zeros to a power of two).
+def f32(x):
+    return float(np.float32(x))
+
+
+def _tree32(vals):
+    if len(vals) == 1:
+        return vals[0]
+    mid = len(vals) // 2
+    return f32(_tree32(vals[:mid]) + _tree32(vals[mid:]))
+
+
+def norm32(vec, w, eps):
+    """Scalar fp32 RMS norm of one row (list of fp32 values as Python floats)."""
+    groups = []
+    for g0 in range(0, len(vec), 4):
+        acc = f32(vec[g0] * vec[g0])
+        for d in range(g0 + 1, g0 + 4):
+            acc = f32(acc + f32(vec[d] * vec[d]))
+        groups.append(acc)
+    width = 1
+    while width < len(groups):
+        width *= 2
+    ss = _tree32(groups + [0.0] * (width - len(groups)))
+    ms = f32(ss / len(vec))
+    r = f32(1.0 / f32(math.sqrt(f32(ms + f32(eps)))))
+    return [f32(f32(vec[d] * r) * _f(w[d])) for d in range(len(vec))]
+
+
+def rope32(vec, cos_row, sin_row):
+    """Scalar fp32 NeoX rotary of one row: rounded products, then one rounded add / subtract."""
+    half = len(vec) // 2
+    outv = list(vec)
+    for d in range(half):
+        c, s_ = _f(cos_row[d]), _f(sin_row[d])
+        a, b2 = vec[d], vec[d + half]
+        outv[d] = f32(f32(a * c) - f32(b2 * s_))
+        outv[d + half] = f32(f32(b2 * c) + f32(a * s_))
+    return outv
 
 
 def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
@@ -108,12 +154,12 @@ def brute_forward(inputs, attrs, present_key, present_value, share_buffer):
                     pv[b][g][j] = inputs["past_value"][b, g, j].copy()
         for g in range(Nkv):
             for i in range(S):
-                kr = [_f(x) for x in k[b, i, g * H:(g + 1) * H]]
+                kr = [_f(x) for x in k[b, i, g * H:(g + 1) * H]]   # exact: T is fp16 or fp32
                 vr = [_f(x) for x in v[b, i, g * H:(g + 1) * H]]
                 if kw is not None:
-                    kr = norm(kr, kw)
+                    kr = norm32(kr, kw, eps)
                 if rotary:
-                    kr = rope(kr, past + i)
+                    kr = rope32(kr, cosc[past + i], sinc[past + i])
                 pk[b][g][past + i] = store(kr, g, "k_scale")
                 pv[b][g][past + i] = store(vr, g, "v_scale")
                 if separate:
