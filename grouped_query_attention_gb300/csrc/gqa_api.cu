@@ -21,8 +21,6 @@
 
 struct gqa_handle {
   gqa_attrs attrs;
-  void* zeroed_ws;          // workspace whose header (status + tickets) is known to be zero
-  size_t zeroed_bytes;
   // per-launch profiling (gqa_profile_begin / gqa_profile_end)
   bool profiling;
   std::vector<cudaEvent_t> events;  // 2 per launch
@@ -441,8 +439,6 @@ gqa_status gqa_create(const gqa_attrs* a, gqa_handle** out) {
   gqa_handle* h = new (std::nothrow) gqa_handle;
   if (!h) return fail(GQA_ERR_INVALID_ARGUMENT, "out of host memory");
   h->attrs = *a;
-  h->zeroed_ws = nullptr;
-  h->zeroed_bytes = 0;
   h->profiling = false;
   h->used = 0;
   *out = h;
@@ -483,12 +479,11 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
     return fail(GQA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, pl.total_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   bind_workspace(&pl, ws);
-  if (h->zeroed_ws != ws || h->zeroed_bytes < pl.hdr_bytes) {
-    cudaError_t e = cudaMemsetAsync(ws, 0, pl.hdr_bytes, st);
-    if (e != cudaSuccess) return cuda_fail(e, "workspace header init");
-    h->zeroed_ws = ws;
-    h->zeroed_bytes = pl.hdr_bytes;
-  }
+  // The header (status word, merge tickets) is cleared by every call: the
+  // caller may reuse the workspace for anything between calls, and a call
+  // that timed out leaves tickets behind.
+  cudaError_t eh = cudaMemsetAsync(ws, 0, pl.hdr_bytes, st);
+  if (eh != cudaSuccess) return cuda_fail(eh, "workspace header clear");
   const gqa::Params& P = pl.P;
   cudaError_t e = cudaSuccess;
   gqa::TmaMaps maps;   // host work of the tensor-core launches, done before the first launch

@@ -176,11 +176,15 @@ GQA_API gqa_status gqa_workspace_size(const gqa_handle* handle, const gqa_inputs
  * Present rows that are not appended (or copied) keep their bytes. Output
  * rows i >= total_b of a prompt without past (padding) are written as 0.
  * workspace: device buffer of at least gqa_workspace_size bytes, 256-byte
- * aligned, owned by the caller, not used concurrently by another call.
+ * aligned, owned by the caller, not used concurrently by another call. Its
+ * contents need not survive between calls: every call first clears the
+ * workspace header (status word and split-merge tickets) on `stream`, so the
+ * caller may use the buffer for anything else in between.
  * Host-side checks as in gqa_workspace_size. Data errors found on the device
  * (seqlens_k[b]+1 outside [S or 1, min(C, total_sequence_length)], a rotary
  * position beyond the cos/sin rows) skip that batch entry without any write
- * out of bounds and set a bit of the workspace's status word. */
+ * out of bounds and set a bit of the workspace's status word, which then
+ * describes this call until the next call on the same workspace clears it. */
 GQA_API gqa_status gqa_forward(gqa_handle* handle, const gqa_inputs* in, const gqa_outputs* out,
                        void* workspace, size_t workspace_bytes, void* stream);
 
@@ -209,10 +213,10 @@ GQA_API gqa_status gqa_forward(gqa_handle* handle, const gqa_inputs* in, const g
 GQA_API gqa_status gqa_forward_noalloc(gqa_handle* handle, const gqa_inputs* in, const gqa_outputs* out,
                                        void* stream);
 
-/* Synchronise `stream`, read and clear the status word that kernels of
- * earlier gqa_forward calls set in `workspace`. *status receives the OR of
- * GQA_DEVICE_* bits (0 = no data error). Returns DEVICE_STATUS if it is
- * non-zero, CUDA on a runtime failure. */
+/* Synchronise `stream`, read and clear the status word that the kernels of
+ * the most recent gqa_forward call on `workspace` set (each call clears it
+ * first). *status receives the OR of GQA_DEVICE_* bits (0 = no data error).
+ * Returns DEVICE_STATUS if it is non-zero, CUDA on a runtime failure. */
 #define GQA_DEVICE_BAD_SEQLEN 1u  /* seqlens_k out of range for the cache / total length / S */
 #define GQA_DEVICE_BAD_ROTARY 2u  /* a rotary position is not covered by cos/sin_cache rows */
 #define GQA_DEVICE_TIMEOUT 4u     /* a bounded pipeline wait gave up (kernel returned early) */
