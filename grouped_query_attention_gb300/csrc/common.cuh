@@ -76,6 +76,59 @@ __device__ __forceinline__ unsigned quant_i4_nibble(float x, float s) {
   return static_cast<unsigned>(static_cast<int>(t) + 8);
 }
 
+// ---- fp32 recipe of the rows stored in the cache (RMS norm, then NeoX rotary)
+// Every operation is one IEEE fp32 rounding and none is fused, so the stored
+// bytes do not depend on which kernel (or lane layout) appends a row: the
+// squares of four consecutive coordinates are summed left to right, the H/4
+// group sums are added as a pairwise tree (neighbours first; a lane butterfly
+// with rising xor distance over lanes that hold consecutive groups computes
+// exactly that tree, zero groups padding it to a power of two),
+// r = 1 / sqrt(ss / H + eps), y = (x r) w, and rotary
+// y[d] = x[d] c - x[d+H/2] s, y[d+H/2] = x[d+H/2] c + x[d] s with each product
+// rounded before the add (com.microsoft.GroupQueryAttention, section Inputs:
+// q/k_norm_weight, cos/sin_cache; section Attributes: qk_norm_epsilon).
+__device__ __forceinline__ float sumsq4_rn(float a, float b, float c, float d) {
+  float s = __fmul_rn(a, a);
+  s = __fadd_rn(s, __fmul_rn(b, b));
+  s = __fadd_rn(s, __fmul_rn(c, c));
+  return __fadd_rn(s, __fmul_rn(d, d));
+}
+
+// Sum of squares of eight consecutive coordinates (two groups, one tree node).
+__device__ __forceinline__ float sumsq8_rn(const float* x) {
+  return __fadd_rn(sumsq4_rn(x[0], x[1], x[2], x[3]), sumsq4_rn(x[4], x[5], x[6], x[7]));
+}
+
+__device__ __forceinline__ float rms_inv_rn(float ss, int H, float eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+}
+
+__device__ __forceinline__ float norm_rn(float x, float r, float w) { return __fmul_rn(__fmul_rn(x, r), w); }
+
+// Rotary of coordinate d < H/2 (x = x[d], partner = x[d+H/2]) and of
+// coordinate d + H/2 (x = x[d+H/2], partner = x[d]).
+__device__ __forceinline__ float rope_first_rn(float x, float partner, float c, float s) {
+  return __fsub_rn(__fmul_rn(x, c), __fmul_rn(partner, s));
+}
+__device__ __forceinline__ float rope_second_rn(float x, float partner, float c, float s) {
+  return __fadd_rn(__fmul_rn(x, c), __fmul_rn(partner, s));
+}
+
+// Sum of squares of a row of H <= 256 fp32 values in shared memory, by one
+// whole warp: lane l holds groups l and l + 32.
+__device__ __forceinline__ float row_sum_squares_warp(const float* row, int H) {
+  const int lane = threadIdx.x & 31;
+  float part[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int d = 4 * (j * 32 + lane);
+    part[j] = d < H ? sumsq4_rn(row[d], row[d + 1], row[d + 2], row[d + 3]) : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) part[j] = __fadd_rn(part[j], __shfl_xor_sync(0xffffffffu, part[j], o));
+  }
+  return __fadd_rn(part[0], part[1]);
+}
+
 __device__ __forceinline__ float channel_scale(const float* sc, int n, int c) {
   return n == 1 ? sc[0] : sc[c];
 }

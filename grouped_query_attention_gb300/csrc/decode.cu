@@ -103,31 +103,21 @@ __device__ void append_row(const Params& p, int b, int g, int i, int j, float* b
   const int lane = threadIdx.x & 31, H = p.H, half = H >> 1;
   const long long src = ((long long)(b * p.S + i) * p.Nkv + g) * H;
   const long long dst = (((long long)b * p.Nkv + g) * p.C + j) * H;
-  // K: RMS norm, rotary at position j, cast or int8 code.
-  float ss = 0.f;
-  for (int d = lane; d < H; d += 32) {
-    float x = load_t(p.k, src + d, p.t_type);
-    buf[d] = x;
-    ss += x * x;
-  }
-  float r = 1.f;
-  if (p.has_norm) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    r = 1.0f / sqrtf(ss / (float)H + p.eps);
-  }
+  // K: RMS norm, rotary at position j, cast or int8 code (the stored-row fp32 recipe).
+  for (int d = lane; d < H; d += 32) buf[d] = load_t(p.k, src + d, p.t_type);
   __syncwarp();
+  const float r = p.has_norm ? rms_inv_rn(row_sum_squares_warp(buf, H), H, p.eps) : 1.f;
   for (int d = lane; d < H; d += 32) {
     float x = buf[d];
-    if (p.has_norm) x = (x * r) * load_t(p.kw, d, p.t_type);
+    if (p.has_norm) x = norm_rn(x, r, load_t(p.kw, d, p.t_type));
     if (p.has_rotary) {
       const int dp = d < half ? d + half : d - half;
       float xp = buf[dp];
-      if (p.has_norm) xp = (xp * r) * load_t(p.kw, dp, p.t_type);
+      if (p.has_norm) xp = norm_rn(xp, r, load_t(p.kw, dp, p.t_type));
       const int dc = d < half ? d : d - half;
       const float c = load_t(p.cos_c, (long long)j * half + dc, p.t_type);
       const float s = load_t(p.sin_c, (long long)j * half + dc, p.t_type);
-      x = d < half ? (x * c - xp * s) : (x * c + xp * s);
+      x = d < half ? rope_first_rn(x, xp, c, s) : rope_second_rn(x, xp, c, s);
     }
     if constexpr (CacheTraits<CacheT>::es == 1)
       reinterpret_cast<int8_t*>(p.present_k)[dst + d] =
@@ -214,31 +204,21 @@ decode_kernel(const Params p) {
     }
     const int i = r / p.G, h = g * p.G + r % p.G;
     const long long src = ((long long)(b * p.S + i) * p.N + h) * H;
-    float ss = 0.f;
-    for (int d = lane; d < H; d += 32) {
-      float x = load_t(p.q, src + d, p.t_type);
-      buf[d] = x;
-      ss += x * x;
-    }
-    float rn = 1.f;
-    if (p.has_norm) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      rn = 1.0f / sqrtf(ss / (float)H + p.eps);
-    }
+    for (int d = lane; d < H; d += 32) buf[d] = load_t(p.q, src + d, p.t_type);
     __syncwarp();
+    const float rn = p.has_norm ? rms_inv_rn(row_sum_squares_warp(buf, H), H, p.eps) : 1.f;
     const int pos = past + i, half = H >> 1;
     for (int d = lane; d < H; d += 32) {
       float x = buf[d];
-      if (p.has_norm) x = (x * rn) * load_t(p.qw, d, p.t_type);
+      if (p.has_norm) x = norm_rn(x, rn, load_t(p.qw, d, p.t_type));
       if (p.has_rotary) {
         const int dp = d < half ? d + half : d - half;
         float xp = buf[dp];
-        if (p.has_norm) xp = (xp * rn) * load_t(p.qw, dp, p.t_type);
+        if (p.has_norm) xp = norm_rn(xp, rn, load_t(p.qw, dp, p.t_type));
         const int dc = d < half ? d : d - half;
         const float cs = load_t(p.cos_c, (long long)pos * half + dc, p.t_type);
         const float sn = load_t(p.sin_c, (long long)pos * half + dc, p.t_type);
-        x = d < half ? (x * cs - xp * sn) : (x * cs + xp * sn);
+        x = d < half ? rope_first_rn(x, xp, cs, sn) : rope_second_rn(x, xp, cs, sn);
       }
       x *= qscale;
       if constexpr (ES == 1) x *= channel_scale(p.k_scale, p.k_scale_n, g * H + d);  // int8 K dequant folded in

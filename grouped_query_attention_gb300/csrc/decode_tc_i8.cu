@@ -280,24 +280,28 @@ __device__ __forceinline__ uint4 f_to_h8(const float* f) {
 __device__ __forceinline__ void norm_rope8(const Params& p, float* lo, float* hi, const float* wlo, const float* whi,
                                            bool norm, bool rope, const float* c, const float* sv) {
   if (norm) {
-    float ss = 0.f;
+    // The stored-row fp32 recipe: lane l8 holds groups 2 l8, 2 l8 + 1 (lo) and
+    // 16 + 2 l8, 17 + 2 l8 (hi); xor distances 1, 2, 4 build the subtrees of
+    // the two halves, which are added last.
+    float slo = sumsq8_rn(lo), shi = sumsq8_rn(hi);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ss += lo[k] * lo[k] + hi[k] * hi[k];
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rn = 1.0f / sqrtf(ss / (float)kHD + p.eps);
+    for (int o = 1; o < 8; o <<= 1) {
+      slo = __fadd_rn(slo, __shfl_xor_sync(0xffffffffu, slo, o));
+      shi = __fadd_rn(shi, __shfl_xor_sync(0xffffffffu, shi, o));
+    }
+    const float rn = rms_inv_rn(__fadd_rn(slo, shi), kHD, p.eps);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      lo[k] = (lo[k] * rn) * wlo[k];
-      hi[k] = (hi[k] * rn) * whi[k];
+      lo[k] = norm_rn(lo[k], rn, wlo[k]);
+      hi[k] = norm_rn(hi[k], rn, whi[k]);
     }
   }
   if (rope) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float a = lo[k], b = hi[k];
-      lo[k] = a * c[k] - b * sv[k];
-      hi[k] = b * c[k] + a * sv[k];
+      lo[k] = rope_first_rn(a, b, c[k], sv[k]);
+      hi[k] = rope_second_rn(b, a, c[k], sv[k]);
     }
   }
 }

@@ -165,24 +165,15 @@ prepass_kernel(const Params p) {
     src = reinterpret_cast<const T*>(role == kKey ? p.k : p.v) + ((long long)(b * p.S + i) * p.Nkv + head) * H;
 
   float* buf = rowbuf[warp];
-  float ss = 0.f;
   for (int d0 = lane * V; d0 < H; d0 += 32 * V) {
     float x[V];
     load_vec<T>(src + d0, x);
 #pragma unroll
-    for (int k = 0; k < V; ++k) {
-      buf[d0 + k] = x[k];
-      ss += x[k] * x[k];
-    }
-  }
-  const bool norm = p.has_norm && role != kValue;
-  float r = 1.f;
-  if (norm) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    r = 1.0f / sqrtf(ss / (float)H + p.eps);
+    for (int k = 0; k < V; ++k) buf[d0 + k] = x[k];
   }
   __syncwarp();
+  const bool norm = p.has_norm && role != kValue;
+  const float r = norm ? rms_inv_rn(row_sum_squares_warp(buf, H), H, p.eps) : 1.f;
   const T* w = reinterpret_cast<const T*>(role == kQuery ? p.qw : p.kw);
   const int half = H >> 1;
   for (int d0 = lane * V; d0 < H; d0 += 32 * V) {
@@ -191,15 +182,15 @@ prepass_kernel(const Params p) {
     for (int k = 0; k < V; ++k) {
       const int d = d0 + k;
       float x = buf[d];
-      if (norm) x = (x * r) * load_t(w, d, p.t_type);
+      if (norm) x = norm_rn(x, r, load_t(w, d, p.t_type));
       if (rotate) {
         const int dp = d < half ? d + half : d - half;
         float xp = buf[dp];
-        if (norm) xp = (xp * r) * load_t(w, dp, p.t_type);
+        if (norm) xp = norm_rn(xp, r, load_t(w, dp, p.t_type));
         const int dc = d < half ? d : d - half;
         const float c = rot_t(p.cos_c, (long long)pos * half + dc, p.t_type);
         const float s = rot_t(p.sin_c, (long long)pos * half + dc, p.t_type);
-        x = d < half ? (x * c - xp * s) : (x * c + xp * s);
+        x = d < half ? rope_first_rn(x, xp, c, s) : rope_second_rn(x, xp, c, s);
       }
       y[k] = x;
     }
@@ -274,16 +265,16 @@ prepass_vec_kernel(const Params p) {
       float xr[V];
       load_vec<T>(reinterpret_cast<const T*>(&raw[u]), xr);
       if (role != kValue && p.has_norm) {
-        float ss = 0.f;
+        // Lane cl holds the groups of coordinates 4 * (V/4 * cl) ..: the rising
+        // xor distances add neighbouring subtrees (the stored-row recipe).
+        float ss = V == 8 ? sumsq8_rn(xr) : sumsq4_rn(xr[0], xr[1], xr[2], xr[3]);
 #pragma unroll
-        for (int k = 0; k < V; ++k) ss += xr[k] * xr[k];
-#pragma unroll
-        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
-        const float rn = 1.0f / sqrtf(ss / (float)H + p.eps);
+        for (int o = 1; o < LPR; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(gmask, ss, o));
+        const float rn = rms_inv_rn(ss, H, p.eps);
         float w[V];
         load_vec<T>(reinterpret_cast<const T*>(role == kQuery ? p.qw : p.kw) + d0, w);
 #pragma unroll
-        for (int k = 0; k < V; ++k) xr[k] = (xr[k] * rn) * w[k];
+        for (int k = 0; k < V; ++k) xr[k] = norm_rn(xr[k], rn, w[k]);
       }
       if (role != kValue && p.has_rotary) {
         const bool first = cl < LPR / 2;
@@ -295,7 +286,7 @@ prepass_vec_kernel(const Params p) {
 #pragma unroll
         for (int k = 0; k < V; ++k) {
           const float xp = __shfl_xor_sync(gmask, xr[k], LPR / 2);
-          y[k] = first ? (xr[k] * c[k] - xp * sn[k]) : (xr[k] * c[k] + xp * sn[k]);
+          y[k] = first ? rope_first_rn(xr[k], xp, c[k], sn[k]) : rope_second_rn(xr[k], xp, c[k], sn[k]);
         }
 #pragma unroll
         for (int k = 0; k < V; ++k) xr[k] = y[k];

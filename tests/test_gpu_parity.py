@@ -5,14 +5,16 @@ ragged tail in both regimes (fused split-KV decode for up to 8 query rows per
 KV head, or 16 on the tensor-core decode; pre-pass + flash prefill
 otherwise). The five workloads run at full size with the
 launch configuration the benchmark uses; their outputs are checked on
-sampled rows the oracle computes one by one and their caches in full.
+sampled rows the oracle computes one by one (for the prefill workloads every
+row of one whole KV-head group and the last 64 positions of every head) and
+their caches in full, byte for byte.
 """
 
 import numpy as np
 import pytest
 
 from grouped_query_attention_gb300.inputs import WORKLOADS, CaseSpec, generate
-from tests.parity import check_caches, check_output, run_gpu, run_oracle, sample_rows
+from tests.parity import check_caches, check_output, run_gpu, run_oracle, sample_rows, valid_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -97,6 +99,14 @@ PREFILL = {
     "i8_per_channel_prompt_h64_g8": spec(dtype="f32", H=64, N=16, Nkv=2, S=70, mode="prompt", capacity=80,
                                          seqlens_k=(69, 33, 1), seqlens_range=None, quant="PER_CHANNEL"),
     "f16_h256_g2": spec(H=256, N=4, Nkv=2, S=20, capacity=500, seqlens_range=(20, 480)),
+    # head sizes whose group count (H/4) is not a power of two: the generic pre-pass pads the
+    # norm's pairwise tree with zero groups; H = 192 in fp32 spreads a row over two lane blocks
+    "f16_h48_norm_rotary_generic_prepass": spec(H=48, N=4, Nkv=2, S=9, capacity=300, seqlens_range=(9, 290),
+                                                qk_norm=True, rotary_theta=1e4),
+    "f32_h80_norm_rotary_i8": spec(dtype="f32", H=80, N=4, Nkv=2, S=6, capacity=300, seqlens_range=(6, 290),
+                                   qk_norm=True, rotary_theta=1e4, quant="PER_CHANNEL", scale_range=(0.01, 0.03)),
+    "f32_h192_norm_rotary": spec(dtype="f32", H=192, N=4, Nkv=2, S=7, capacity=300, seqlens_range=(7, 290),
+                                 qk_norm=True, rotary_theta=1e4),
     "f16_h128_g8_s65": spec(N=16, Nkv=2, S=65, seqlens_range=(65, 700), rotary_theta=1e4, qk_norm=True),
     "f16_copy_s12": spec(S=12, N=8, Nkv=2, mode="copy", past_len=300, seqlens_range=(11, 311)),
     "f32_bidirectional_prompt_s33": spec(dtype="f32", N=4, Nkv=2, S=33, mode="prompt", capacity=33, causal=0,
@@ -187,10 +197,32 @@ def test_decode_idempotent_repeat():
     _check(case, repeat=2)
 
 
+def full_size_sample(case, n_random=48):
+    """Output rows compared at full size: random rows and the last row of every batch entry;
+    for a prefill (S > 1) also every row of the last KV-head group of the last batch entry
+    (all its positions and heads: late key tiles, both query tiles of a CTA, lazy rescales
+    across 4096 keys) and the last 64 positions of every head (the last query tiles)."""
+    rows = set(sample_rows(case, n_random, seed=1))
+    inp = case["inputs"]
+    B, S = inp["query"].shape[:2]
+    N, Nkv = case["attrs"]["num_heads"], case["attrs"]["kv_num_heads"]
+    G = N // Nkv
+    if S > 1:
+        ok = valid_rows(case)
+        b_last = B - 1
+        for h in range((Nkv - 1) * G, N):
+            rows.update((b_last, h, i) for i in np.nonzero(ok[b_last])[0])
+        for b in range(B):
+            live = np.nonzero(ok[b])[0]
+            for h in range(N):
+                rows.update((b, h, int(i)) for i in live[-64:])
+    return sorted(rows)
+
+
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_workload_full_size(name):
     case = generate(WORKLOADS[name], seed=0)
-    sample = None if name == "prompt_f32_b1_s16" else sample_rows(case, 48, seed=1)
+    sample = None if name == "prompt_f32_b1_s16" else full_size_sample(case)
     _check(case, sample=sample)
 
 
