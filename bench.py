@@ -11,6 +11,10 @@ TFLOP/s (4*H per visible query/key pair).
 
 --impl reference times the CPU oracle (fp64 numpy) on the host cores on a
 bounded sample of the same workload.
+The headline line (value, roofline, e2e, clocks, cpu_baseline) is the
+default workload; the same measurements of the other configurations (tiny
+fp32 prompt, fp16 causal prefill, fp16 chunked prefill, fp32 decode over an
+int8 cache) follow under "workloads" (--workloads none skips them).
 Under torchrun (N>1) every rank runs an independent replica on its own GPU
 (the operator has no cross-GPU exchange); value = units of all ranks / max time.
 """
@@ -264,14 +268,16 @@ def _slice_batches(case, nb: int) -> dict:
 
 # --------------------------------------------------------------------------- GPU arm
 
-def run_gpu_arm(args, world, rank, local) -> None:
+def measure_workload(name: str, args, world: int, rank: int, local: int) -> dict:
+    """Times one workload on this rank's GPU: device-resident steps (value, per-kernel events,
+    roofline), the same steps end to end with host buffers (e2e), clocks, and on rank 0 at N=1
+    the oracle on a bounded sample (cpu_baseline)."""
     import torch
 
     from grouped_query_attention_gb300 import GroupQueryAttention, capi
 
-    torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    case = generate(WORKLOADS[args.workload], seed=rank)
+    case = generate(WORKLOADS[name], seed=rank)
     sp = case["spec"]
     inp = case["inputs"]
     wk = work(case)
@@ -309,7 +315,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
         flush_l2()
         step()
     torch.cuda.synchronize()
-    assert op.device_status() == 0, "device status set during warm-up"
+    assert op.device_status() == 0, f"{name}: device status set during warm-up"
 
     # Clock sampling: a short soak of the same step keeps the GPU busy while
     # nvidia-smi samples, then the K timed steps run inside the same window.
@@ -346,7 +352,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
     dom_ms = max_over_ranks(sum(per_kernel[dominant]) / len(per_kernel[dominant]), world, device)
     ms_local = sum(times_ms) / len(times_ms)
     ms = max_over_ranks(ms_local, world, device)
-    assert op.device_status() == 0, "device status set during the timed steps"
+    assert op.device_status() == 0, f"{name}: device status set during the timed steps"
 
     # ---- end to end through the public API with host buffers (pinned), copies in the timed region
     host_in = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory() for k in ("query", "key", "value", "seqlens_k")}
@@ -360,8 +366,8 @@ def run_gpu_arm(args, world, rank, local) -> None:
     for k in range(args.steps):
         flush_l2()
         e_starts[k].record(stream)
-        for name, t in host_in.items():
-            dev[name].copy_(t, non_blocking=True)
+        for key_name, t in host_in.items():
+            dev[key_name].copy_(t, non_blocking=True)
         step()
         host_out.copy_(out, non_blocking=True)
         e_ends[k].record(stream)
@@ -380,7 +386,14 @@ def run_gpu_arm(args, world, rank, local) -> None:
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
                   "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"], "bias_stage": ["prepass.cu"]}[dominant]
     peak_key = "hbm_gbs" if wk["bound"] == "hbm" else "bf16_tflops"
-    if dominant == "window_shift":
+    latency_bound = wk["units"] * 1e12 < 1e9 if wk["kind"] == "prefill" else False
+    if latency_bound:
+        # A few thousand flops per launch: the launch latency is the bound, no roofline applies.
+        wk["bound"] = "latency"
+        achieved = wk["flops"] / (dom_ms / 1e3) / 1e12
+        peak = None
+        unit = "TFLOP/s"
+    elif dominant == "window_shift":
         # The window shift of a sliding-window cache: bytes of the rows it moves, read and written.
         wk["bound"] = "hbm"
         achieved = window_shift_bytes(case) / (dom_ms / 1e3) / 1e9
@@ -403,7 +416,7 @@ def run_gpu_arm(args, world, rank, local) -> None:
         achieved = wk["flops"] / (dom_ms / 1e3) / 1e12
         peak = float(peaks["bf16_tflops"])
         unit = "TFLOP/s"
-    traffic = recorded_traffic(args.workload, kernel_src)
+    traffic = recorded_traffic(name, kernel_src)
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -411,22 +424,18 @@ def run_gpu_arm(args, world, rank, local) -> None:
         cpu_baseline.pop("seconds", None)
         cpu_baseline.pop("runs", None)
 
-    if rank != 0:
-        return
-    line = {
-        "metric": METRIC,
+    if wk["bound"] == "latency":
+        peak_source = "none (launch-latency bound)"
+    elif wk["bound"] == "alu":
+        peak_source = f"derived ({peak_key})"
+    else:
+        peak_source = f"{peaks_src} ({peak_key}, burst)"
+    rec = {
         "value": round(value, 3),
         "unit": wk["unit"],
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": round(ms, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
         "dtype": "f16" if sp.dtype == "f16" else "f32",
-        "data": "synthetic (seeded numpy, shapes and distributions of the workload)",
-        "config": {"workload": args.workload, "batch": sp.B, "seq_len": sp.S, "num_heads": sp.N,
+        "config": {"workload": name, "batch": sp.B, "seq_len": sp.S, "num_heads": sp.N,
                    "kv_num_heads": sp.Nkv, "head_size": sp.H, "capacity": sp.capacity,
                    "cache": (f"{sp.quant} int{sp.bits}" if sp.quant != "NONE" else (sp.cache_dtype or sp.dtype)),
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then read back)",
@@ -434,10 +443,8 @@ def run_gpu_arm(args, world, rank, local) -> None:
                    "regime": "decode" if plan.regime == 1 else "prefill",
                    "split_len": int(plan.split_len), "max_splits": int(plan.max_splits)},
         "roofline": {"bound": wk["bound"], "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": (f"derived ({peak_key})" if wk["bound"] == "alu"
-                                     else f"{peaks_src} ({peak_key}, burst)"),
-                     "kernel": dominant, "kernel_ms": round(dom_ms, 5)},
+                     "frac": round(achieved / peak, 4) if peak else None, "traffic": traffic,
+                     "peak_source": peak_source, "kernel": dominant, "kernel_ms": round(dom_ms, 5)},
         "kernels_ms": {k: round(sum(v) / len(v), 5) for k, v in per_kernel.items()},
         "e2e": {"value": round(e2e_value, 3), "unit": wk["unit"], "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
@@ -446,6 +453,57 @@ def run_gpu_arm(args, world, rank, local) -> None:
                    "samples": clocks["samples"]},
         "cpu_baseline": cpu_baseline,
     }
+    op.close()
+    del dev, pk, pv, out, ws, flush, flush_words, call, opt
+    torch.cuda.empty_cache()
+    return rec
+
+
+# The workloads of the other configurations reported beside the headline one:
+# the tiny fp32 prompt (launch latency), fp16 causal prefill (tensor cores),
+# fp16 chunked prefill (tensor cores) and fp32 decode over an int8 cache (HBM).
+CONFIG_WORKLOADS = ["prompt_f32_b1_s16", "prefill_f16_b4_s4096", "chunked_prefill_f16_b8_s512",
+                    "decode_int8_f32_b32_c16384"]
+
+
+def run_gpu_arm(args, world, rank, local) -> None:
+    import torch
+
+    torch.cuda.set_device(local)
+    rec = measure_workload(args.workload, args, world, rank, local)
+    extra = {}
+    names = CONFIG_WORKLOADS if args.workloads == "configs" else \
+        ([] if args.workloads == "none" else [w for w in args.workloads.split(",") if w])
+    for w in names:
+        if w != args.workload:
+            extra[w] = measure_workload(w, args, world, rank, local)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": rec["value"],
+        "unit": rec["unit"],
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": rec["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": rec["dtype"],
+        "data": "synthetic (seeded numpy, shapes and distributions of the workload)",
+        "config": rec["config"],
+        "roofline": rec["roofline"],
+        "kernels_ms": rec["kernels_ms"],
+        "e2e": rec["e2e"],
+        "gpu_launches": rec["gpu_launches"] + sum(r["gpu_launches"] for r in extra.values()),
+        "clocks": rec["clocks"],
+        "cpu_baseline": rec["cpu_baseline"],
+    }
+    if extra:
+        # Every other configuration, measured in this run the same way (its own clocks,
+        # roofline of its dominant kernel, end-to-end value and oracle sample).
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
 
 
@@ -503,6 +561,9 @@ def main() -> None:
     ap.add_argument("--soak", type=float, default=1.5, help="seconds of untimed load for clock sampling")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle timing for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default="configs",
+                    help="other workloads measured in the same run and reported under 'workloads': "
+                         "'configs' (the other configurations), 'none', or a comma-separated list")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)      # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()
