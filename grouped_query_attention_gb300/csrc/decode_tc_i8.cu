@@ -468,29 +468,57 @@ __device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, i
   }
 }
 
-// One K row of an int8 tile as fp16 pairs in 64 tensor-memory columns of this
-// thread's lane (lane = key row; warp w owns lanes 32 (w % 4) ..).
-__device__ __forceinline__ void convert_k_row_to_tmem(const uint8_t* src, int t, uint32_t taddr) {
+// Eight int8 codes (one 16-byte chunk, xor 0x80 applied by the caller's
+// load) as eight fp16 values in four 32-bit words: the byte c + 128 as the low
+// mantissa bits of 1024.0 (fp16 0x6400) is 1152 + c exactly.
+__device__ __forceinline__ void codes_to_h8(uint32_t w0, uint32_t w1, uint32_t* h) {
   const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+  const uint32_t wv[2] = {w0 ^ 0x80808080u, w1 ^ 0x80808080u};
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t p01 = __byte_perm(wv[k], 0x64646464u, 0x4140u);
+    const uint32_t p23 = __byte_perm(wv[k], 0x64646464u, 0x4342u);
+    const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&p01), bias);
+    const __half2 b2 = __hsub2(*reinterpret_cast<const __half2*>(&p23), bias);
+    h[2 * k] = *reinterpret_cast<const uint32_t*>(&a);
+    h[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+}
+
+// One converter step: row t of the int8 K tile `ksrc` into fp16 pairs in 64
+// tensor-memory columns of this thread's lane, and (when `vsrc` is not null)
+// row t of the int8 V tile of the previous tile into the fp16 operand tile
+// `vdst`. The loads of both rows are issued together, half a row at a time,
+// so the two conversions overlap instead of running one after the other.
+__device__ __forceinline__ void convert_kv_rows(const uint8_t* ksrc, const uint8_t* vsrc, uint8_t* vdst, int t,
+                                                uint32_t taddr) {
 #pragma unroll
   for (int hlf = 0; hlf < 2; ++hlf) {
+    uint4 kw[4], vw[4];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) kw[c4] = *reinterpret_cast<const uint4*>(ksrc + sw128_offset(t, 4 * hlf + c4));
+    if (vsrc) {
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) vw[c4] = *reinterpret_cast<const uint4*>(vsrc + sw128_offset(t, 4 * hlf + c4));
+    }
     uint32_t h[32];
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {   // chunk c = 4 hlf + c4: codes 16c .. 16c+15
-      const int c = 4 * hlf + c4;
-      const uint4 w = *reinterpret_cast<const uint4*>(src + sw128_offset(t, c));
-      const uint32_t wv[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t p01 = __byte_perm(wv[k], 0x64646464u, 0x4140u);
-        const uint32_t p23 = __byte_perm(wv[k], 0x64646464u, 0x4342u);
-        const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&p01), bias);
-        const __half2 b2 = __hsub2(*reinterpret_cast<const __half2*>(&p23), bias);
-        h[8 * c4 + 2 * k] = *reinterpret_cast<const uint32_t*>(&a);
-        h[8 * c4 + 2 * k + 1] = *reinterpret_cast<const uint32_t*>(&b2);
-      }
+    for (int c4 = 0; c4 < 4; ++c4) {
+      codes_to_h8(kw[c4].x, kw[c4].y, h + 8 * c4);
+      codes_to_h8(kw[c4].z, kw[c4].w, h + 8 * c4 + 4);
     }
     tmem_st32(taddr + 32 * hlf, h);
+    if (vsrc) {
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {   // chunk c: codes 16c .. 16c+15 -> fp16 columns 16c ..
+        uint32_t v[8];
+        codes_to_h8(vw[c4].x, vw[c4].y, v);
+        codes_to_h8(vw[c4].z, vw[c4].w, v + 4);
+        const int col = 16 * (4 * hlf + c4), bx = col >> 6, ch = (col & 63) >> 3;
+        *reinterpret_cast<uint4*>(vdst + bx * kBox + sw128_offset(t, ch)) = make_uint4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<uint4*>(vdst + bx * kBox + sw128_offset(t, ch + 1)) = make_uint4(v[4], v[5], v[6], v[7]);
+      }
+    }
   }
 }
 
@@ -792,23 +820,29 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       const DItem it = sm.item[slot];
       if (it.end) break;
       for (int t = 0; t < it.ntiles; ++t, ++u) {
+        // One step converts K(u) and V(u - 1) together (one set of waits,
+        // one fence, interleaved loads).
         const int st = u % kNS, kb = u & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[st], (uint32_t)(u / kNS) & 1u) &&
-                                         mbar_wait(&sm.k16empty[kb], ((uint32_t)(u >> 1) & 1u) ^ 1u)) ||
-            aborted(sm)) {
+        const bool with_v = uv < u;
+        const int sv = uv % kNSV, vb = uv & 1;
+        bool ready = mbar_wait(&sm.kfull[st], (uint32_t)(u / kNS) & 1u) &&
+                     mbar_wait(&sm.k16empty[kb], ((uint32_t)(u >> 1) & 1u) ^ 1u);
+        if (with_v)
+          ready = ready && mbar_wait(&sm.vfull[sv], (uint32_t)(uv / kNSV) & 1u) &&
+                  mbar_wait(&sm.v16empty[vb], ((uint32_t)(uv >> 1) & 1u) ^ 1u);
+        if (!__all_sync(0xffffffffu, ready) || aborted(sm)) {
           ok = false;
           break;
         }
-        convert_k_row_to_tmem(sm.k8[st], ct, tmem + lane_addr + kKCol + kb * 64);
+        convert_kv_rows(sm.k8[st], with_v ? sm.v8[sv] : nullptr, sm.v[vb], ct, tmem + lane_addr + kKCol + kb * 64);
         tmem_st_wait();
         tc_fence_before();
+        if (with_v) fence_async_smem();
         mbar_arrive(&sm.k16full[kb]);
         mbar_arrive(&sm.kempty[st]);
-        if (uv < u) {
-          if (!convert_v(uv)) {
-            ok = false;
-            break;
-          }
+        if (with_v) {
+          mbar_arrive(&sm.v16full[vb]);
+          mbar_arrive(&sm.vempty[sv]);
           ++uv;
         }
       }
