@@ -92,15 +92,26 @@ __device__ __forceinline__ float rcp_approx(float x) {
 //   softcap c:  c * tanh(raw * scale / c) * log2(e) + bias * log2(e), with
 //               tanh(u) = 1 - 2 / (exp(2u) + 1): e2 = exp2(raw * k_exp),
 //               x = c log2(e) - 2 c log2(e) / (e2 + 1).
-//   softcap, |u| = |raw * scale / c| <= 1/2 (every lane of a warp): the
+//   softcap, |u| = |raw * scale / c| <= 1/4 (every lane of a warp): the
 //               same value on the FMA pipe, c tanh(u) log2(e) =
 //               raw * scale * log2(e) * P(u^2), P below.
+// tanh(u) / u = P(u^2) for |u| <= 1/4: degree-3 least-squares fit in z = u^2
+// over [0, 1/16] (Chebyshev nodes, weighted for relative error), coefficients
+// rounded to fp32: relative error 3.6e-9 in exact arithmetic.
+constexpr float kTanhP1 = -3.333323896e-01f;
+constexpr float kTanhP2 = 1.332412809e-01f;
+constexpr float kTanhP3 = -5.141825974e-02f;
+
 struct ScoreConst {
   float k_raw;    // raw multiplier: scale * log2(e) (no softcap) or 2 * scale * log2(e) / c
   float k_mul;    // -2 c log2(e)
   float k_add;    // c log2(e)
-  float k_u;      // scale / c
-  float k_w;      // scale * log2(e)
+  // Softcap on the FMA pipe in terms of the raw product x (u = x scale / c):
+  // c tanh(u) log2(e) = x Q(x^2), Q(y) = sum_n C_n y^n with
+  // C_n = scale log2(e) P_n (scale / c)^(2n) (P_0 = 1), so neither u nor the
+  // final scale costs an operation per score.
+  float c3[4];
+  float y3;       // validity: x^2 <= (1/16) (c / scale)^2, i.e. |u| <= 1/4
 };
 
 __device__ __forceinline__ ScoreConst score_const(const Params& p) {
@@ -108,35 +119,28 @@ __device__ __forceinline__ ScoreConst score_const(const Params& p) {
   k.k_raw = p.softcap > 0.f ? 2.0f * kLog2e * p.scale / p.softcap : p.scale * kLog2e;
   k.k_mul = -2.0f * p.softcap * kLog2e;
   k.k_add = p.softcap * kLog2e;
-  k.k_u = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
-  k.k_w = p.scale * kLog2e;
+  const float ku = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
+  const float ku2 = ku * ku, kw = p.scale * kLog2e;
+  const float p3[4] = {1.f, kTanhP1, kTanhP2, kTanhP3};
+  float pw = 1.f;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    k.c3[n] = kw * p3[n] * pw;
+    pw *= ku2;
+  }
+  k.y3 = ku2 > 0.f ? 0.0625f / ku2 : INFINITY;
   return k;
 }
 
-// tanh(u) / u = P(u^2) for |u| <= 1/2: degree-5 least-squares fit in z = u^2
-// over [0, 1/4] (Chebyshev nodes, weighted for relative error), coefficients
-// rounded to fp32: relative error 3.5e-9 in exact arithmetic, about 1.2 fp32
-// ulps when evaluated by Horner's rule in fp32.
-constexpr float kTanhP1 = -3.333332539e-01f;
-constexpr float kTanhP2 = 1.333289742e-01f;
-constexpr float kTanhP3 = -5.389288813e-02f;
-constexpr float kTanhP4 = 2.127229236e-02f;
-constexpr float kTanhP5 = -6.609579083e-03f;
-
-// Softcapped score of two raw products on the FMA pipe plus `add` (the bias
-// in the log2 domain) in the last fused multiply-add (valid for |u| <= 1/2;
-// z = u^2 is returned for the check), log2 domain.
-__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k, float2& z, float2 add) {
-  const float2 zero = make_float2(0.f, 0.f);
-  const float2 u = ffma2(raw, make_float2(k.k_u, k.k_u), zero);
-  z = ffma2(u, u, zero);
-  float2 q = ffma2(z, make_float2(kTanhP5, kTanhP5), make_float2(kTanhP4, kTanhP4));
-  q = ffma2(q, z, make_float2(kTanhP3, kTanhP3));
-  q = ffma2(q, z, make_float2(kTanhP2, kTanhP2));
-  q = ffma2(q, z, make_float2(kTanhP1, kTanhP1));
-  q = ffma2(q, z, make_float2(1.f, 1.f));
-  const float2 w = ffma2(raw, make_float2(k.k_w, k.k_w), zero);
-  return ffma2(w, q, add);
+// Softcapped scores of two raw products on the FMA pipe, log2 domain, plus
+// `add` (the bias in the log2 domain) in the last fused multiply-add; the
+// squared raw products are returned for the validity check (x^2 <= y3).
+__device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k, float2& y, float2 add) {
+  y = ffma2(raw, raw, make_float2(0.f, 0.f));
+  float2 q = ffma2(y, make_float2(k.c3[3], k.c3[3]), make_float2(k.c3[2], k.c3[2]));
+  q = ffma2(q, y, make_float2(k.c3[1], k.c3[1]));
+  q = ffma2(q, y, make_float2(k.c3[0], k.c3[0]));
+  return ffma2(raw, q, add);
 }
 
 
@@ -520,8 +524,8 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           tmem_ld32(s_addr + hf * 64 + 32, r + 32);
           tmem_ld_wait();
           // Transform the half in place: scale, softcap, bias. With a softcap the
-          // FMA-pipe polynomial goes first and is checked afterwards (|u| <= 1/2
-          // on every lane of the warp, from the largest u^2); otherwise the raw
+          // FMA-pipe polynomial goes first and is checked afterwards (|u| <= 1/4
+          // on every lane of the warp, from the largest raw^2); otherwise the raw
           // scores are read again from tensor memory (intact: P of this half is
           // written after it) and take the exp2 / reciprocal form.
           auto transform = [&](bool poly) -> float {
@@ -552,9 +556,9 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 #pragma unroll
                   for (int e = 0; e < 16; e += 2) {
                     float2 z;
-                    const float2 y = softcap_poly2(
-                        make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1])), kc, z,
-                        make_float2(ba[e], ba[e + 1]));
+                    const float2 raw2 = make_float2(__uint_as_float(r[c + c16 + e]), __uint_as_float(r[c + c16 + e + 1]));
+                    const float2 bias2 = make_float2(ba[e], ba[e + 1]);
+                    const float2 y = softcap_poly2(raw2, kc, z, bias2);
                     r[c + c16 + e] = __float_as_uint(y.x);
                     r[c + c16 + e + 1] = __float_as_uint(y.y);
                     zmax = fmax3(zmax, z.x, z.y);
@@ -591,7 +595,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           };
           if constexpr (CAP) {
             const float zmax = transform(true);
-            if (__any_sync(0xffffffffu, !(zmax <= 0.25f))) {
+            if (__any_sync(0xffffffffu, !(zmax <= kc.y3))) {
               tmem_ld32(s_addr + hf * 64, r);
               tmem_ld32(s_addr + hf * 64 + 32, r + 32);
               tmem_ld_wait();
