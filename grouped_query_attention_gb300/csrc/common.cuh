@@ -99,8 +99,12 @@ __device__ __forceinline__ float sumsq8_rn(const float* x) {
   return __fadd_rn(sumsq4_rn(x[0], x[1], x[2], x[3]), sumsq4_rn(x[4], x[5], x[6], x[7]));
 }
 
+// 1 / sqrt(ss / H + eps), each step one IEEE rounding. For a power-of-two H
+// the division is the (exact) product with 1/H, and 1 / x rounded to nearest
+// is the correctly rounded reciprocal: the same values with fewer instructions.
 __device__ __forceinline__ float rms_inv_rn(float ss, int H, float eps) {
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+  const float ms = (H & (H - 1)) == 0 ? __fmul_rn(ss, 1.0f / (float)H) : __fdiv_rn(ss, (float)H);
+  return __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
 __device__ __forceinline__ float norm_rn(float x, float r, float w) { return __fmul_rn(__fmul_rn(x, r), w); }
@@ -127,6 +131,38 @@ __device__ __forceinline__ float row_sum_squares_warp(const float* row, int H) {
     for (int o = 1; o < 32; o <<= 1) part[j] = __fadd_rn(part[j], __shfl_xor_sync(0xffffffffu, part[j], o));
   }
   return __fadd_rn(part[0], part[1]);
+}
+
+// RMS norm (weights wlo / whi, when `norm`) and then rotary (cos c / sin s,
+// when c is not null) of one 128-value row spread over 8 lanes: lane l8 of the
+// row holds dims 8 l8 .. 8 l8 + 7 (lo) and 64 + 8 l8 .. (hi), so the NeoX
+// partner of every value is in the same lane. The 8 lanes are consecutive
+// lanes of the warp and every lane of the warp calls (shuffles). Same fp32
+// recipe as the stored rows (groups of four, pairwise tree).
+__device__ __forceinline__ void norm_rope_row8(float* lo, float* hi, const float* wlo, const float* whi, bool norm,
+                                               const float* c, const float* s, float eps) {
+  if (norm) {
+    float slo = sumsq8_rn(lo), shi = sumsq8_rn(hi);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      slo = __fadd_rn(slo, __shfl_xor_sync(0xffffffffu, slo, o));
+      shi = __fadd_rn(shi, __shfl_xor_sync(0xffffffffu, shi, o));
+    }
+    const float rn = rms_inv_rn(__fadd_rn(slo, shi), 128, eps);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      lo[k] = norm_rn(lo[k], rn, wlo[k]);
+      hi[k] = norm_rn(hi[k], rn, whi[k]);
+    }
+  }
+  if (c) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float a = lo[k], b = hi[k];
+      lo[k] = rope_first_rn(a, b, c[k], s[k]);
+      hi[k] = rope_second_rn(b, a, c[k], s[k]);
+    }
+  }
 }
 
 __device__ __forceinline__ float channel_scale(const float* sc, int n, int c) {

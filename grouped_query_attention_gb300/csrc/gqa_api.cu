@@ -5,8 +5,9 @@
 //   decode regime (S * G <= 8, head size 64/128): [copy of live past rows in
 //     copy mode] -> one fused split-KV decode launch (append + attention +
 //     merge);
-//   prefill regime: [copy] -> pre-pass (append K/V, prepared queries into the
-//     workspace) -> flash prefill.
+//   prefill regime: [copy] -> pre-pass (append K/V; prepared queries into the
+//     workspace for the CUDA-core prefill, the tensor-core prefill prepares
+//     its own) -> [bias staging] -> flash prefill.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -334,8 +335,13 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
     if (!gqa::prefill_simt_supported(P) || !gqa::prepass_supported(P))
       return fail(GQA_ERR_UNSUPPORTED, "no prefill kernel for head_size %lld", H);
     pl->tensor_core = !window && gqa::prefill_tc_supported(P);
+    // The tensor-core prefill loads the raw query rows of a tile (when the
+    // group size divides its 128 rows) and applies norm / rotary itself;
+    // otherwise the pre-pass prepares fp16 queries for it, and fp32 ones for
+    // the CUDA-core prefill.
+    P.q_in_prefill = pl->tensor_core && 128 % G == 0 ? 1 : 0;
     P.qprep_type = pl->tensor_core ? gqa::kF16 : gqa::kF32;
-    pl->qprep_bytes = align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
+    pl->qprep_bytes = P.q_in_prefill ? 0 : align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
     if (separate) pl->kvsep_bytes = 2 * align_up((size_t)B * Nkv * S * H * (tdt == GQA_F16 ? 2 : 4));
     if (pl->tensor_core && gqa::prefill_tc_bias_staged(P)) {
       pl->bias_staged = true;

@@ -58,6 +58,8 @@ struct Params {
   unsigned int* status;  // OR of GQA_DEVICE_* bits
   void* qprep;           // prepared queries, layout [B][N_kv][S*G][H]
   int qprep_type;        // ElemType of qprep
+  int q_in_prefill;      // 1: the tensor-core prefill loads raw query rows and applies norm / rotary
+                         // itself (no qprep; the pre-pass appends K/V only)
   float* bias_stage;     // bias * log2(e) as fp32 rows of bias_stage_ld floats ([bdim*S] rows) for the
   int bias_stage_ld;     // tensor-core prefill's TMA bias staging (16-byte row stride), else null
   void* kv_sep_k;        // kv_separate: new K/V rows in T as attention reads them, [B][N_kv][S][H]

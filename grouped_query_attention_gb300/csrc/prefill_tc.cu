@@ -62,7 +62,8 @@ struct __align__(1024) TcSmem {
   uint8_t k[kNS][kTile];
   uint8_t v[kNS][kTile];
   float bias[kNS][kBiasRows][kBN];                // staged bias rows, fp32 times log2(e)
-  uint64_t q_full;
+  uint64_t q_land[2];           // query tile t copied (TMA)
+  uint64_t q_ready[2];          // query tile t rewritten in place (norm / rotary by the softmax threads)
   uint64_t k_full[kNS], v_full[kNS], kv_empty[kNS];
   uint64_t bias_full[kNS], bias_empty[kNS];
   uint64_t s_full[2], p_full[2], o_done[2];
@@ -184,6 +185,117 @@ __device__ __forceinline__ void set_abort(const Params& p, TcSmem& sm) {
   flag_status(p, GQA_DEVICE_TIMEOUT_BIT);
 }
 
+// Eight fp16 values (16 bytes) as fp32, and back (round to nearest).
+__device__ __forceinline__ void ld_h8f(const __half* src, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(src);
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 v = __half22float2(h[k]);
+    f[2 * k] = v.x;
+    f[2 * k + 1] = v.y;
+  }
+}
+
+__device__ __forceinline__ uint4 f_to_h8(const float* f) {
+  uint4 u;
+  __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) h[k] = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+  return u;
+}
+
+// RMS norm and rotary of one query row held by 8 lanes (lane l8: dims 8 l8 ..
+// and 64 + 8 l8 ..), as packed fp32 pairs with fused multiply-adds: queries
+// feed only the scores (no stored bytes depend on them), so they need no
+// fixed rounding order. `ns` holds the negated sines.
+__device__ __forceinline__ void norm_rope_q8(float2* lo, float2* hi, const float2* wlo, const float2* whi, bool norm,
+                                             const float2* c, const float2* ns, float eps) {
+  const float2 zero = make_float2(0.f, 0.f);
+  if (norm) {
+    float2 acc = zero;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = ffma2(lo[k], lo[k], acc);
+      acc = ffma2(hi[k], hi[k], acc);
+    }
+    float ss = acc.x + acc.y;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rn = rsqrtf(ss * (1.0f / 128.0f) + eps);
+    const float2 rn2 = make_float2(rn, rn);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      lo[k] = ffma2(lo[k], ffma2(wlo[k], rn2, zero), zero);
+      hi[k] = ffma2(hi[k], ffma2(whi[k], rn2, zero), zero);
+    }
+  }
+  if (c) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = lo[k], b = hi[k];
+      lo[k] = ffma2(b, ns[k], ffma2(a, c[k], zero));             // a c - b s
+      hi[k] = ffma2(a, make_float2(-ns[k].x, -ns[k].y), ffma2(b, c[k], zero));   // b c + a s
+    }
+  }
+}
+
+// In-place query preparation (q_in_prefill with RMS norm and / or rotary):
+// the TMA warp loads the raw query rows of the CTA's two tiles, row r of the
+// (b, g) block = (position i = r / G, head g G + r % G), already in the
+// 128-byte-swizzled K-major layout the S MMA reads; these threads rewrite
+// them as norm, then rotary at the absolute position past + i, fp16
+// (com.microsoft.GroupQueryAttention, section Inputs: q_norm_weight,
+// cos/sin_cache; section Implementation variants: rotary flash prefill
+// rotates query blocks at their absolute positions). `wt` = 0..255 over the
+// softmax threads: 8 lanes per row, 32 rows per pass, four passes per tile;
+// the cos/sin rows are loaded before the wait for the tile, and ready[t] is
+// arrived (one arrival per warp) once tile t is rewritten. Rows past the
+// block hold zeros (the copy's fill) and stay zero.
+__device__ void transform_q_tiles(const Params& p, TcSmem& sm, int past, int r0, int nrows, int wt) {
+  const int l8 = wt & 7, sub = wt >> 3, lane = wt & 31;
+  float2 wlo[4], whi[4];
+  if (p.has_norm) {
+    ld_h8f(reinterpret_cast<const __half*>(p.qw) + 8 * l8, reinterpret_cast<float*>(wlo));
+    ld_h8f(reinterpret_cast<const __half*>(p.qw) + 64 + 8 * l8, reinterpret_cast<float*>(whi));
+  }
+  const __half* cbase = reinterpret_cast<const __half*>(p.cos_c);
+  const __half* sbase = reinterpret_cast<const __half*>(p.sin_c);
+  for (int tile = 0; tile < 2; ++tile) {
+    uint4 cs[4], sn[4];
+    if (p.has_rotary) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int r = min(r0 + tile * kBM + k * 32 + sub, nrows - 1);
+        const long long cb = (long long)(past + r / p.G) * (kHD / 2) + 8 * l8;
+        cs[k] = __ldg(reinterpret_cast<const uint4*>(cbase + cb));
+        sn[k] = __ldg(reinterpret_cast<const uint4*>(sbase + cb));
+      }
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_land[tile], 0)) && lane == 0) set_abort(p, sm);
+    uint8_t* qt = sm.q[tile];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rl = k * 32 + sub;              // row inside the tile
+      float2 lo[4], hi[4], c[4], ns[4];
+      ld_h8f(reinterpret_cast<const __half*>(qt + sw128_offset(rl, l8)), reinterpret_cast<float*>(lo));
+      ld_h8f(reinterpret_cast<const __half*>(qt + kBox + sw128_offset(rl, l8)), reinterpret_cast<float*>(hi));
+      if (p.has_rotary) {
+        const uint4 nsn = make_uint4(sn[k].x ^ 0x80008000u, sn[k].y ^ 0x80008000u, sn[k].z ^ 0x80008000u,
+                                     sn[k].w ^ 0x80008000u);   // negated fp16 sines
+        ld_h8f(reinterpret_cast<const __half*>(&cs[k]), reinterpret_cast<float*>(c));
+        ld_h8f(reinterpret_cast<const __half*>(&nsn), reinterpret_cast<float*>(ns));
+      }
+      norm_rope_q8(lo, hi, wlo, whi, p.has_norm != 0, p.has_rotary ? c : nullptr, ns, p.eps);
+      *reinterpret_cast<uint4*>(qt + sw128_offset(rl, l8)) = f_to_h8(reinterpret_cast<const float*>(lo));
+      *reinterpret_cast<uint4*>(qt + kBox + sw128_offset(rl, l8)) = f_to_h8(reinterpret_cast<const float*>(hi));
+    }
+    fence_async_smem();   // rewritten tile (generic stores) -> async proxy: the S MMAs may read it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.q_ready[tile]);
+  }
+}
+
 // MODE (PrefillMode): kPlain has no softcap and no bias (the scores are the
 // scaled products); kGeneric reads the bias per thread; kStagedBias adds the
 // bias loader warp. CAP: softcap > 0 (compile-time, so that the 32 scores of
@@ -233,7 +345,10 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 
   if (warp == 1) tmem_alloc(&sm.tmem, 512);
   if (tid == 0) {
-    mbar_init(&sm.q_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.q_land[t], 1);
+      mbar_init(&sm.q_ready[t], 8);   // one arrival per softmax warp
+    }
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
@@ -259,6 +374,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
   const int qrow0 = bg * nrows + r0;                 // row of Q0 in the prepared-query matrix
+  const bool qx = p.q_in_prefill && (p.has_norm || p.has_rotary);   // query tiles rewritten in place
   const int krow0 = bg * (p.kv_separate ? p.S : p.C) + kmin;   // row of the first key in the K/V matrix
 
   if (warp == 0) {
@@ -269,9 +385,15 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     // (fp32 times log2(e)), keys j0 .. j0+127; keys past the bias row read 0.
     const int brow0 = STAGED ? (p.bias_bdim > 1 ? b : 0) * p.S + i_lo : 0;
     if (elect_one()) {
-      mbar_arrive_tx(&sm.q_full, 2 * kTile);
-      for (int q = 0; q < 2; ++q)
-        for (int bx = 0; bx < 2; ++bx) tma_load_2d(sm.q[q] + bx * kBox, &tmq, bx * 64, qrow0 + q * kBM, &sm.q_full);
+      for (int q = 0; q < 2; ++q) {
+        mbar_arrive_tx(&sm.q_land[q], kTile);
+        for (int bx = 0; bx < 2; ++bx) {
+          if (p.q_in_prefill)   // raw query rows: positions (r0 + 128 q) / G .., heads g G ..
+            tma_load_4d(sm.q[q] + bx * kBox, &tmq, bx * 64, g * p.G, (r0 + q * kBM) / p.G, b, &sm.q_land[q]);
+          else                  // queries prepared by the pre-pass
+            tma_load_2d(sm.q[q] + bx * kBox, &tmq, bx * 64, qrow0 + q * kBM, &sm.q_land[q]);
+        }
+      }
     }
     __syncwarp();
     int issued = 0, issued_b = 0;
@@ -305,7 +427,8 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       }
     }
     // Drain: no copy of this CTA may still be landing when it exits.
-    mbar_wait(&sm.q_full, 0);
+    mbar_wait(&sm.q_land[0], 0);
+    mbar_wait(&sm.q_land[1], 0);
     for (int t = max(0, issued_b - kNS); t < issued_b; ++t)
       mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u);
     for (int t = max(0, issued - kNS); t < issued; ++t) {
@@ -342,11 +465,21 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       for (int ks = 0; ks < 8; ++ks) mma_f16_ts(d, pa + ks * 8, b0 + (uint64_t)(ks * 128), kIdO, acc || ks > 0);
       mma_commit(&sm.o_done[q]);
     };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.k_full[0], 0));
+    // Query tile t is ready once copied, or once rewritten in place when the
+    // softmax threads apply norm / rotary; S_0(0) may start before tile 1 is.
+    uint64_t* qready = qx ? sm.q_ready : sm.q_land;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&qready[0], 0) && mbar_wait(&sm.k_full[0], 0));
     if (ok) {
       if (elect_one()) {
         tc_fence_after();
         issue_s(0, 0);
+      }
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, mbar_wait(&qready[1], 0));
+    }
+    if (ok) {
+      if (elect_one()) {
+        tc_fence_after();
         issue_s(1, 0);
       }
       __syncwarp();
@@ -429,6 +562,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
                  (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
                      p.bias_ld;
     const int brow = live ? i - i_lo : 0;     // staged bias row of this thread (any in-range row when not live)
+    if (qx) transform_q_tiles(p, sm, past, r0, nrows, tid - 64);
     const ScoreConst kc = score_const(p);
     float m_run = kNegBig, l_run = 0.f;
     bool ok = true;
@@ -733,16 +867,21 @@ bool prefill_tc_supported(const Params& p) {
 }
 
 cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps) {
-  const long long qrows = (long long)p.B * p.Nkv * p.S * p.G;
   const long long krows = (long long)p.B * p.Nkv * (p.kv_separate ? p.S : p.C);
-  cudaError_t e = encode_fp16_2d_sw128(&maps->m[0], p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   const void* ksrc = p.kv_separate ? p.kv_sep_k : p.present_k;
   const void* vsrc = p.kv_separate ? p.kv_sep_v : p.present_v;
   if ((e = encode_fp16_2d_sw128(&maps->m[1], ksrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
     return e;
   if ((e = encode_fp16_2d_sw128(&maps->m[2], vsrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
     return e;
+  if (p.q_in_prefill) {
+    if ((e = encode_fp16_query_sw128(&maps->m[0], p.q, p.B, p.S, p.N, (uint32_t)p.G)) != cudaSuccess) return e;
+  } else {
+    const long long qrows = (long long)p.B * p.Nkv * p.S * p.G;
+    if ((e = encode_fp16_2d_sw128(&maps->m[0], p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM)) != cudaSuccess)
+      return e;
+  }
   maps->m[3] = maps->m[2];   // a valid map in the bias slot when nothing is staged (never read)
   if (!prefill_tc_bias_staged(p)) return cudaSuccess;
   return encode_f32_2d(&maps->m[3], p.bias_stage, (uint64_t)p.bias_bdim * p.S, (uint64_t)p.bias_ld,

@@ -47,6 +47,25 @@ __device__ __forceinline__ void load_vec<__half>(const __half* src, float* dst) 
   }
 }
 
+// The same from a 16-byte chunk already in registers (passed by value, so no
+// local-memory copy is needed).
+template <typename T>
+__device__ __forceinline__ void unpack_vec(uint4 v, float* dst);
+template <>
+__device__ __forceinline__ void unpack_vec<float>(uint4 v, float* dst) {
+  dst[0] = __uint_as_float(v.x); dst[1] = __uint_as_float(v.y); dst[2] = __uint_as_float(v.z); dst[3] = __uint_as_float(v.w);
+}
+template <>
+__device__ __forceinline__ void unpack_vec<__half>(uint4 v, float* dst) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    dst[2 * k] = f.x;
+    dst[2 * k + 1] = f.y;
+  }
+}
+
 // Store V consecutive fp32 values as DstT (round to nearest), 16/8-byte stores.
 template <typename DstT, int V>
 __device__ __forceinline__ void store_n(DstT* dst, const float* src) {
@@ -124,7 +143,7 @@ prepass_kernel(const Params p) {
   __shared__ float rowbuf[kWarpsPerBlock][kMaxH];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long kv_rows = (long long)p.B * p.S * p.Nkv;
-  const long long q_rows = (long long)p.B * p.S * p.N;
+  const long long q_rows = p.q_in_prefill ? 0 : (long long)p.B * p.S * p.N;   // the prefill may prepare its queries
   const long long row = (long long)blockIdx.x * kWarpsPerBlock + warp;
   if (row >= 2 * kv_rows + q_rows) return;
 
@@ -205,120 +224,189 @@ prepass_kernel(const Params p) {
   }
 }
 
-// Vectorised pre-pass for rows of at most 32 16-byte chunks. One block per
-// token (b, i) handles its 2*N_kv + N_q rows (K rows, V rows, query rows);
-// LPR = H / V lanes per row (V elements per 16-byte chunk), 256 / LPR row
-// groups per block, each taking kUnroll rows per pass with their loads issued
-// together. The rotary partner (d +- H/2) is chunk lane ^ LPR/2, read with one
-// shuffle per element; norm weights and cos/sin rows are 16-byte vector loads.
-constexpr int kUnroll = 4;
+// Vectorised pre-pass. Rows are numbered token-major, row = token * nrow + r
+// with r < N_kv a K row, N_kv <= r < 2 N_kv a V row and the rest query rows
+// (none when the prefill prepares its own); nrow = 2*N_kv + N_q. A row group
+// of LPR = H / (2 V) lanes (V elements per 16-byte chunk) takes one row at a
+// time, striding over the grid's row groups; lane l holds the chunk of dims
+// l V .. (lo) and the one of dims H/2 + l V .. (hi), so the NeoX rotary
+// partner of every value is in the same lane and one cos / sin chunk serves
+// both. The loads of the group's next row are issued before the current row
+// is computed. Norm weights are loaded once.
+__host__ __device__ inline int prepass_rows_per_token(const Params& p) { return 2 * p.Nkv + (p.q_in_prefill ? 0 : p.N); }
+constexpr int kPrepassBlocksPerSm = 3;
+
+// Where a row is: row = tok * nrow + r, tok = b * S + i. Kept incrementally
+// (no integer division per row).
+struct RowPos {
+  int tok, r, b, i;
+};
+
+__device__ __forceinline__ RowPos row_pos(long long row, int nrow, int S) {
+  RowPos q;
+  q.tok = (int)(row / nrow);
+  q.r = (int)(row - (long long)q.tok * nrow);
+  q.b = q.tok / S;
+  q.i = q.tok - q.b * S;
+  return q;
+}
+
+// The position `stride` rows further, stride = st_tok * nrow + st_r.
+__device__ __forceinline__ RowPos row_advance(RowPos q, int st_tok, int st_r, int nrow, int S) {
+  q.r += st_r;
+  int dt = st_tok;
+  if (q.r >= nrow) {
+    q.r -= nrow;
+    ++dt;
+  }
+  q.tok += dt;
+  q.i += dt;
+  if (q.i >= S) {
+    q.b += q.i / S;
+    q.i %= S;
+  }
+  return q;
+}
+
+// A lane's part of one row: its lo and hi chunks and the batch length.
+struct RowLoads {
+  uint4 lo, hi;
+  int total;        // seqlens_k[b] + 1
+};
 
 template <typename T, typename CacheT, typename QT, int H>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(256, kPrepassBlocksPerSm)
 prepass_vec_kernel(const Params p) {
   constexpr int V = Vec<T>::n;
-  constexpr int LPR = H / V;            // lanes per row (power of two, <= 32)
+  constexpr int LPR = H / (2 * V);      // lanes per row (power of two, <= 16)
   constexpr int GROUPS = 256 / LPR;     // row groups per block
-  static_assert(LPR >= 2 && LPR <= 32 && (LPR & (LPR - 1)) == 0, "row layout");
+  static_assert(LPR >= 1 && LPR <= 16 && (LPR & (LPR - 1)) == 0, "row layout");
   const int lane = threadIdx.x & 31;
-  const int grp = threadIdx.x / LPR, cl = threadIdx.x % LPR;
-  const unsigned gmask = (LPR == 32) ? 0xffffffffu : (((1u << LPR) - 1u) << ((lane / LPR) * LPR));
-  const int tok = blockIdx.x;
-  const int b = tok / p.S, i = tok - b * p.S;
-  const int nrow = 2 * p.Nkv + p.N;
-  const int d0 = cl * V;
-  const T* qsrc = reinterpret_cast<const T*>(p.q) + (long long)tok * p.N * H + d0;
-  const T* ksrc = reinterpret_cast<const T*>(p.k) + (long long)tok * p.Nkv * H + d0;
-  const T* vsrc = reinterpret_cast<const T*>(p.v) + (long long)tok * p.Nkv * H + d0;
-  const int total = p.seqlens[b] + 1;
+  const int cl = threadIdx.x % LPR;
+  const unsigned gmask = LPR == 32 ? 0xffffffffu : (((1u << LPR) - 1u) << ((lane / LPR) * LPR));
+  const int nrow = prepass_rows_per_token(p);
+  const long long nrows = (long long)p.B * p.S * nrow;
+  const long long stride = (long long)gridDim.x * GROUPS;
+  const int dlo = cl * V, dhi = H / 2 + cl * V;   // this lane's dims, and the cos / sin columns dlo ..
+  // Norm weights of this lane's chunks (K and query rows), loaded once, kept raw.
+  uint4 wk_lo = make_uint4(0, 0, 0, 0), wk_hi = wk_lo, wq_lo = wk_lo, wq_hi = wk_lo;
+  if (p.has_norm) {
+    wk_lo = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.kw) + dlo);
+    wk_hi = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.kw) + dhi);
+    if (!p.q_in_prefill) {
+      wq_lo = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.qw) + dlo);
+      wq_hi = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.qw) + dhi);
+    }
+  }
+  auto issue = [&](const RowPos& q, RowLoads& l) {
+    const int r = q.r;
+    const T* src = r < p.Nkv ? reinterpret_cast<const T*>(p.k) + ((long long)q.tok * p.Nkv + r) * H
+                   : r < 2 * p.Nkv ? reinterpret_cast<const T*>(p.v) + ((long long)q.tok * p.Nkv + r - p.Nkv) * H
+                                   : reinterpret_cast<const T*>(p.q) + ((long long)q.tok * p.N + r - 2 * p.Nkv) * H;
+    l.lo = *reinterpret_cast<const uint4*>(src + dlo);
+    l.hi = *reinterpret_cast<const uint4*>(src + dhi);
+    l.total = p.seqlens[q.b] + 1;
+  };
 
-  for (int r0 = grp; r0 < nrow; r0 += GROUPS * kUnroll) {
-    // Loads of all rows of this pass first (addresses need no lengths), kept
-    // as raw 16-byte chunks until used.
-    uint4 raw[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int r = r0 + u * GROUPS;
-      if (r >= nrow) continue;
-      const T* src = r < p.Nkv ? ksrc + (long long)r * H
-                     : r < 2 * p.Nkv ? vsrc + (long long)(r - p.Nkv) * H
-                                     : qsrc + (long long)(r - 2 * p.Nkv) * H;
-      raw[u] = *reinterpret_cast<const uint4*>(src);
+  long long row = (long long)blockIdx.x * GROUPS + threadIdx.x / LPR;
+  const int st_tok = (int)(stride / nrow), st_r = (int)(stride - (long long)st_tok * nrow);
+  RowPos pc = row_pos(row, nrow, p.S), pn = pc;
+  RowLoads cur, nxt;
+  if (row < nrows) issue(pc, cur);
+  for (; row < nrows; row += stride) {   // uniform over the row group
+    if (row + stride < nrows) {
+      pn = row_advance(pc, st_tok, st_r, nrow, p.S);
+      issue(pn, nxt);
     }
-    const int past = batch_past(p, total);
-    if (past < 0) {
-      if (i == 0 && threadIdx.x == 0 && r0 == grp) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
-      return;   // the whole block (one token) is skipped
-    }
+    const int r = pc.r, b = pc.b, i = pc.i;
+    const int past = batch_past(p, cur.total);
+    const int role = r < p.Nkv ? kKey : (r < 2 * p.Nkv ? kValue : kQuery);
+    const int head = role == kKey ? r : (role == kValue ? r - p.Nkv : r - 2 * p.Nkv);
     const int pos = past + i;                                 // absolute position (rotary)
-    const int crow = batch_rows(p, total, past).keep + i;     // cache row
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int r = r0 + u * GROUPS;
-      if (r >= nrow) continue;
-      const int role = r < p.Nkv ? kKey : (r < 2 * p.Nkv ? kValue : kQuery);
-      const int head = role == kKey ? r : (role == kValue ? r - p.Nkv : r - 2 * p.Nkv);
-      if (role != kValue && p.has_rotary && pos >= p.rotary_rows) {
-        if (cl == 0) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
-        continue;   // every lane of the row group takes this branch together
+    const bool rot = p.has_rotary && role != kValue;
+    if (past < 0) {   // the token is skipped
+      if (i == 0 && r == 0 && cl == 0) flag_status(p, GQA_DEVICE_BAD_SEQLEN_BIT);
+    } else if (rot && pos >= p.rotary_rows) {
+      if (cl == 0) flag_status(p, GQA_DEVICE_BAD_ROTARY_BIT);
+    } else {
+      uint4 cr = make_uint4(0, 0, 0, 0), sr = cr;
+      if (rot) {   // cos / sin rows are shared by the heads of a token (cache hits after the first)
+        cr = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.cos_c) + (long long)pos * (H / 2) + dlo));
+        sr = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.sin_c) + (long long)pos * (H / 2) + dlo));
       }
-      float xr[V];
-      load_vec<T>(reinterpret_cast<const T*>(&raw[u]), xr);
+      const int crow = batch_rows(p, cur.total, past).keep + i;   // cache row
+      float lo[V], hi[V];
+      unpack_vec<T>(cur.lo, lo);
+      unpack_vec<T>(cur.hi, hi);
       if (role != kValue && p.has_norm) {
-        // Lane cl holds the groups of coordinates 4 * (V/4 * cl) ..: the rising
-        // xor distances add neighbouring subtrees (the stored-row recipe).
-        float ss = V == 8 ? sumsq8_rn(xr) : sumsq4_rn(xr[0], xr[1], xr[2], xr[3]);
+        // The stored-row recipe: the lo chunks of the row's lanes are the
+        // groups of the first half, the hi chunks those of the second; rising
+        // xor distances add neighbouring subtrees of each half, then the halves.
+        float slo = V == 8 ? sumsq8_rn(lo) : sumsq4_rn(lo[0], lo[1], lo[2], lo[3]);
+        float shi = V == 8 ? sumsq8_rn(hi) : sumsq4_rn(hi[0], hi[1], hi[2], hi[3]);
 #pragma unroll
-        for (int o = 1; o < LPR; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(gmask, ss, o));
-        const float rn = rms_inv_rn(ss, H, p.eps);
-        float w[V];
-        load_vec<T>(reinterpret_cast<const T*>(role == kQuery ? p.qw : p.kw) + d0, w);
-#pragma unroll
-        for (int k = 0; k < V; ++k) xr[k] = norm_rn(xr[k], rn, w[k]);
-      }
-      if (role != kValue && p.has_rotary) {
-        const bool first = cl < LPR / 2;
-        const int dc = (first ? cl : cl - LPR / 2) * V;
-        float c[V], sn[V];
-        load_vec<T>(reinterpret_cast<const T*>(p.cos_c) + (long long)pos * (H / 2) + dc, c);
-        load_vec<T>(reinterpret_cast<const T*>(p.sin_c) + (long long)pos * (H / 2) + dc, sn);
-        float y[V];
+        for (int o = 1; o < LPR; o <<= 1) {
+          slo = __fadd_rn(slo, __shfl_xor_sync(gmask, slo, o));
+          shi = __fadd_rn(shi, __shfl_xor_sync(gmask, shi, o));
+        }
+        const float rn = rms_inv_rn(__fadd_rn(slo, shi), H, p.eps);
+        float wl[V], wh[V];
+        unpack_vec<T>(role == kQuery ? wq_lo : wk_lo, wl);
+        unpack_vec<T>(role == kQuery ? wq_hi : wk_hi, wh);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
-          const float xp = __shfl_xor_sync(gmask, xr[k], LPR / 2);
-          y[k] = first ? rope_first_rn(xr[k], xp, c[k], sn[k]) : rope_second_rn(xr[k], xp, c[k], sn[k]);
+          lo[k] = norm_rn(lo[k], rn, wl[k]);
+          hi[k] = norm_rn(hi[k], rn, wh[k]);
         }
+      }
+      if (rot) {
+        float c[V], sn[V];
+        unpack_vec<T>(cr, c);
+        unpack_vec<T>(sr, sn);
 #pragma unroll
-        for (int k = 0; k < V; ++k) xr[k] = y[k];
+        for (int k = 0; k < V; ++k) {
+          const float a = lo[k], bb = hi[k];
+          lo[k] = rope_first_rn(a, bb, c[k], sn[k]);
+          hi[k] = rope_second_rn(bb, a, c[k], sn[k]);
+        }
       }
       if (role == kQuery) {
         const int g = head / p.G, gi = head - g * p.G;
-        QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H + d0;
-        store_n<QT, V>(dst, xr);
+        QT* dst = reinterpret_cast<QT*>(p.qprep) + (((long long)(b * p.Nkv + g) * p.S + i) * p.G + gi) * H;
+        store_n<QT, V>(dst + dlo, lo);
+        store_n<QT, V>(dst + dhi, hi);
       } else {
-        append_chunk<T, CacheT, V>(p, role, b, head, crow, d0, xr);
+        append_chunk<T, CacheT, V>(p, role, b, head, crow, dlo, lo);
+        append_chunk<T, CacheT, V>(p, role, b, head, crow, dhi, hi);
       }
     }
+    cur = nxt;
+    pc = pn;
   }
 }
 
 template <typename T, typename CacheT, typename QT>
 cudaError_t launch_vec(const Params& p, cudaStream_t st, bool* done) {
   constexpr int V = Vec<T>::n;
-  const long long tokens = (long long)p.B * p.S;
+  const long long rows = (long long)p.B * p.S * prepass_rows_per_token(p);
   auto go = [&](auto kern) {
     *done = true;
-    if (tokens == 0) return cudaSuccess;
-    kern<<<(unsigned)tokens, 256, 0, st>>>(p);
+    if (rows == 0) return cudaSuccess;
+    // One row group per row up to kPrepassBlocksPerSm resident blocks per SM
+    // (152 SMs); beyond that the groups stride over the rows.
+    const long long groups = 256 / (p.H / (2 * V));
+    const long long want = (rows + groups - 1) / groups;
+    const long long cap = 152LL * kPrepassBlocksPerSm;
+    kern<<<(unsigned)(want < cap ? want : cap), 256, 0, st>>>(p);
     return cudaGetLastError();
   };
-  switch (p.H / V) {
-    case 2: return go(prepass_vec_kernel<T, CacheT, QT, 2 * V>);
-    case 4: return go(prepass_vec_kernel<T, CacheT, QT, 4 * V>);
-    case 8: return go(prepass_vec_kernel<T, CacheT, QT, 8 * V>);
-    case 16: return go(prepass_vec_kernel<T, CacheT, QT, 16 * V>);
-    case 32: return go(prepass_vec_kernel<T, CacheT, QT, 32 * V>);
-    default: return cudaSuccess;  // not a power-of-two chunk count: the generic kernel runs
+  switch (p.H / (2 * V)) {   // lanes per row
+    case 1: return go(prepass_vec_kernel<T, CacheT, QT, 2 * V>);
+    case 2: return go(prepass_vec_kernel<T, CacheT, QT, 4 * V>);
+    case 4: return go(prepass_vec_kernel<T, CacheT, QT, 8 * V>);
+    case 8: return go(prepass_vec_kernel<T, CacheT, QT, 16 * V>);
+    case 16: return go(prepass_vec_kernel<T, CacheT, QT, 32 * V>);
+    default: return cudaSuccess;  // not a power of two: the generic kernel runs
   }
 }
 
@@ -447,7 +535,7 @@ cudaError_t launch_prepass(const Params& p, cudaStream_t st) {
   else
     ev = launch_vec<float, float, float>(p, st, &done);
   if (done || ev != cudaSuccess) return ev;
-  const long long rows = (long long)p.B * p.S * (2 * p.Nkv + p.N);
+  const long long rows = (long long)p.B * p.S * prepass_rows_per_token(p);
   const unsigned blocks = (unsigned)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
   if (blocks == 0) return cudaSuccess;
   dim3 grid(blocks), block(kWarpsPerBlock * 32);

@@ -14,6 +14,14 @@ namespace gqa {
 cudaError_t encode_fp16_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                                  uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
 
+// 4D map of a (B, S, N, 128) fp16 query tensor (BSH layout, head size 128)
+// with the 128-byte swizzle: boxes of 64 dims x G heads x 128/G positions x 1
+// batch land as 128 rows of 128 bytes in (position, head) order, the layout of
+// a 64-column K-major MMA operand box; positions past S read as zero.
+// G must divide 128.
+cudaError_t encode_fp16_query_sw128(CUtensorMap* map, const void* base, uint64_t B, uint64_t S, uint64_t N,
+                                    uint32_t G);
+
 // The same for a row-major [rows][cols] matrix of bytes (int8 codes): boxes of
 // box_cols (<= 128) x box_rows bytes with the 128-byte swizzle.
 cudaError_t encode_u8_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
