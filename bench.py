@@ -380,11 +380,14 @@ def measure_workload(name: str, args, world: int, rank: int, local: int) -> dict
     e2e_value = units_all / (e2e_ms / 1e3)
 
     peaks, peaks_src = load_peaks()
+    # The sources a kernel's code comes from (a traffic record holds only while they are unchanged).
+    shared = ["common.cuh", "gqa_internal.h"]
     tc_decode_src = ["decode_tc_i8.cu" if sp.quant != "NONE" else "decode_tc.cu", "tcgen05.cuh"]
     kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": tc_decode_src,
                   "prefill_tensor_core": ["prefill_tc.cu", "tcgen05.cuh"],
                   "prefill_cuda_core": ["prefill_simt.cu"], "prepass": ["prepass.cu"],
-                  "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"], "bias_stage": ["prepass.cu"]}[dominant]
+                  "copy_past": ["prepass.cu"], "window_shift": ["prepass.cu"],
+                  "bias_stage": ["prepass.cu"]}[dominant] + shared
     peak_key = "hbm_gbs" if wk["bound"] == "hbm" else "bf16_tflops"
     latency_bound = wk["units"] * 1e12 < 1e9 if wk["kind"] == "prefill" else False
     if latency_bound:
