@@ -25,7 +25,8 @@ GQA_DEVICE_BAD_SEQLEN, GQA_DEVICE_BAD_ROTARY, GQA_DEVICE_TIMEOUT = 1, 2, 4
 
 EXPORTS = ["gqa_attrs_default", "gqa_create", "gqa_workspace_size", "gqa_forward",
            "gqa_read_device_status", "gqa_describe_plan", "gqa_destroy", "gqa_status_string",
-           "gqa_last_error", "gqa_forward_noalloc", "gqa_profile_begin", "gqa_profile_end"]
+           "gqa_last_error", "gqa_forward_noalloc", "gqa_profile_begin", "gqa_profile_end",
+           "gqa_set_wait_limit"]
 KERNEL_KINDS = {1: "copy_past", 2: "prepass", 3: "decode", 4: "prefill_cuda_core", 5: "prefill_tensor_core",
                 6: "decode_tensor_core", 7: "window_shift", 8: "bias_stage"}
 GQA_REGIME_DECODE, GQA_REGIME_PREFILL = 1, 2
@@ -105,6 +106,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.gqa_profile_end.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_float),
                                     ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
     lib.gqa_profile_end.restype = ctypes.c_int
+    lib.gqa_set_wait_limit.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32]
+    lib.gqa_set_wait_limit.restype = ctypes.c_int
     lib.gqa_destroy.argtypes = [ctypes.c_void_p]
     lib.gqa_destroy.restype = None
     lib.gqa_status_string.argtypes = [ctypes.c_int]
@@ -185,6 +188,11 @@ def gqa_profile_end(handle, capacity: int = 4096) -> list:
     n = ctypes.c_int32()
     _check(load_library().gqa_profile_end(handle, kinds, ms, capacity, ctypes.byref(n)))
     return [(KERNEL_KINDS.get(kinds[i], str(kinds[i])), ms[i]) for i in range(min(n.value, capacity))]
+
+
+def gqa_set_wait_limit(handle, cycles: int, withhold_copy: int = -1) -> None:
+    """Bound of the tensor-core kernels' pipeline waits (0: default) and the timeout-path test switch."""
+    _check(load_library().gqa_set_wait_limit(handle, int(cycles), int(withhold_copy)))
 
 
 def gqa_destroy(handle) -> None:

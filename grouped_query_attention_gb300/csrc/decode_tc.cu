@@ -495,7 +495,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     uint32_t iphase[2] = {0, 0};
     bool ok = true;
     while (true) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iempty[slot], iphase[slot] ^ 1u)) || aborted(sm)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.iempty[slot], iphase[slot] ^ 1u, p.wait_budget)) || aborted(sm)) {
         ok = false;
         break;
       }
@@ -545,9 +545,9 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     // S(u) is done, V(u) after O += V P(u).
     int slot = 0, tau = 0, nk = 0, nv = 0;   // tiles begun; K and V fills issued
     uint32_t iphase[2] = {0, 0};
-    bool ok = true;
+    bool ok = true, withheld = false;
     while (ok) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.imap[slot], iphase[slot]))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.imap[slot], iphase[slot], p.wait_budget))) {
         ok = false;
         break;
       }
@@ -558,14 +558,19 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       for (int t = 0; t < it.ntiles; ++t, ++tau) {
         const int st = tau % kNS;
         const uint32_t par = ((uint32_t)(tau / kNS) & 1u) ^ 1u;
+        if (tau == p.withhold_tile) {   // testing: no copy of this tile, its waits expire
+          withheld = true;
+          ok = false;
+          break;
+        }
         if (!ready && it.j0 + (t + 1) * kKT > it.past) {   // the tile holds new rows
-          if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot]))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&sm.iready[slot], iphase[slot], p.wait_budget))) {
             ok = false;
             break;
           }
           ready = true;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kempty[st], par)) || aborted(sm)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kempty[st], par, p.wait_budget)) || aborted(sm)) {
           ok = false;
           break;
         }
@@ -576,7 +581,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         }
         __syncwarp();
         ++nk;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vempty[st], par)) || aborted(sm)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.vempty[st], par, p.wait_budget)) || aborted(sm)) {
           ok = false;
           break;
         }
@@ -591,11 +596,11 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       iphase[slot] ^= 1u;
       slot ^= 1;
     }
-    if (!ok && lane == 0) set_abort(p, sm);
+    if (!ok && !withheld && lane == 0) set_abort(p, sm);
     // Drain: every fill this warp issued has landed before the CTA can exit
     // (older fills completed before their stage was refilled).
-    for (int u = max(0, nk - kNS); u < nk; ++u) mbar_wait(&sm.kfull[u % kNS], (uint32_t)(u / kNS) & 1u);
-    for (int u = max(0, nv - kNS); u < nv; ++u) mbar_wait(&sm.vfull[u % kNS], (uint32_t)(u / kNS) & 1u);
+    for (int u = max(0, nk - kNS); u < nk; ++u) mbar_wait(&sm.kfull[u % kNS], (uint32_t)(u / kNS) & 1u, p.wait_budget);
+    for (int u = max(0, nv - kNS); u < nv; ++u) mbar_wait(&sm.vfull[u % kNS], (uint32_t)(u / kNS) & 1u, p.wait_budget);
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     int slot = 0, tau = 0;
@@ -616,8 +621,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     }
     auto issue_pv = [&](int u, bool acc) {
       const int st = u % kNS, pb = u & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u) &&
-                                       mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u)))
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[pb], (uint32_t)(u >> 1) & 1u, p.wait_budget) &&
+                                       mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u, p.wait_budget)))
         return false;
       if (elect_one()) {
         tc_fence_after();
@@ -633,7 +638,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       return true;
     };
     while (ok) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.qready[slot], iphase[slot]))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.qready[slot], iphase[slot], p.wait_budget))) {
         ok = false;
         break;
       }
@@ -641,8 +646,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (it.end) break;
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int u = tau + t, st = u % kNS, sb = u & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[st], (uint32_t)(u / kNS) & 1u) &&
-                                         mbar_wait(&sm.s_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.kfull[st], (uint32_t)(u / kNS) & 1u, p.wait_budget) &&
+                                         mbar_wait(&sm.s_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u, p.wait_budget))) {
           ok = false;
           break;
         }
@@ -674,13 +679,13 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     if (!ok && lane == 0) set_abort(p, sm);
     if (elect_one()) {
       mma_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0);
+      mbar_wait(&sm.drain, 0, p.wait_budget);
     }
     __syncwarp();
   } else {
     // ================================================================ softmax
-    // A warp never leaves the loop except right after a named barrier at
-    // which every softmax warp reads the same abort flag.
+    // A warp leaves the loop only on a value reduced at a named barrier
+    // (bar.red.or), so every softmax warp takes the same exit.
     const int quarter = warp & 3;
     const int kl = quarter * 32 + lane;           // tensor-memory lane: key of the tile, dim of O^T
     const int ws = warp - kSoftWarp0;             // softmax warp index 0..3
@@ -689,9 +694,8 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
     int slot = 0, tau = 0, icount = 0;
     uint32_t iphase[2] = {0, 0};
     while (true) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.qready[slot], iphase[slot])) && lane == 0) set_abort(p, sm);
-      named_sync();
-      if (aborted(sm)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.qready[slot], iphase[slot], p.wait_budget)) && lane == 0) set_abort(p, sm);
+      if (named_sync_or(aborted(sm))) break;   // one decision for every softmax warp
       const DItem it = sm.item[slot];
       if (it.end) break;
       const int b = it.b, g = it.g;
@@ -715,7 +719,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         const bool key_ok = jk < it.jend;
         float s[R];
         bool grow_here = false;   // a visible score exceeds its row's reference by more than 2^kLazy
-        bool got = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (uint32_t)(u >> 1) & 1u));
+        bool got = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (uint32_t)(u >> 1) & 1u, p.wait_budget));
         if (got) {
           tc_fence_after();
           uint32_t raw[16];
@@ -725,7 +729,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.s_free[sb]);
           // V rows past the key range may hold any bits: zero them (P is 0 there, 0 * NaN is not).
-          if (!key_ok && !mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u)) set_abort(p, sm);
+          if (!key_ok && !mbar_wait(&sm.vfull[st], (uint32_t)(u / kNS) & 1u, p.wait_budget)) set_abort(p, sm);
           if (!key_ok && !aborted(sm)) {
 #pragma unroll
             for (int bx = 0; bx < 2; ++bx)
@@ -755,8 +759,12 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         }
         // One barrier tells every softmax thread whether any row needs a new
         // reference max (rare after an item's first tile).
-        const bool any_grow = named_sync_or(grow_here);
-        if (aborted(sm)) {
+        // The abort flag may be set by another warp role at any time, so the
+        // softmax warps leave only on a value reduced at a barrier (the same
+        // for all of them); the common case needs one barrier.
+        const bool ab0 = aborted(sm);
+        const bool any_grow = named_sync_or(grow_here || ab0);
+        if (any_grow && named_sync_or(ab0)) {
           bad = true;
           break;
         }
@@ -780,7 +788,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         if (any_grow && t > 0) {
           // O^T must hold P.V up to tile t-1.
           const int pu = u - 1;
-          if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[pu & 1], (uint32_t)(pu >> 1) & 1u))) {
+          if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[pu & 1], (uint32_t)(pu >> 1) & 1u, p.wait_budget))) {
             tc_fence_after();
             uint32_t o[16];
             tmem_ld16(tmem + lane_addr + 32, o);
@@ -803,7 +811,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         for (int r = 0; r < R; ++r)
           if (mt[r] > m_run[r] + kLazy) m_run[r] = mt[r];
         // P^T(u): its buffer is free once P.V(u-2) finished.
-        if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u))) {
+        if (__all_sync(0xffffffffu, mbar_wait(&sm.p_free[sb], ((uint32_t)(u >> 1) & 1u) ^ 1u, p.wait_budget))) {
 #pragma unroll
           for (int r = 0; r < R; ++r) {
             const float pr = ex2(s[r] - m_run[r]);   // masked scores are -inf: 0
@@ -821,7 +829,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
       if (bad) break;
       tau += it.ntiles;
       // ---- end of item: O^T row kl = dim kl of every query row
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.o_full, (uint32_t)icount & 1u));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&sm.o_full, (uint32_t)icount & 1u, p.wait_budget));
       uint32_t o[16];
       if (got) {
         tc_fence_after();
@@ -837,8 +845,7 @@ decode_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const 
         for (int x = 16; x > 0; x >>= 1) l += __shfl_xor_sync(0xffffffffu, l, x);
         if (lane == 0) sm.redl[ws][r] = l;
       }
-      named_sync();
-      if (aborted(sm)) break;
+      if (named_sync_or(aborted(sm))) break;   // one decision for every softmax warp
       const int bg = b * p.Nkv + g;
       if (it.nsplit == 1) {
 #pragma unroll

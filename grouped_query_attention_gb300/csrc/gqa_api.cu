@@ -22,6 +22,8 @@
 
 struct gqa_handle {
   gqa_attrs attrs;
+  long long wait_budget;    // bound of each pipeline wait of the tensor-core kernels (clock cycles)
+  int withhold_tile;        // >= 0: testing the timeout path (see gqa_set_wait_limit)
   // per-launch profiling (gqa_profile_begin / gqa_profile_end)
   bool profiling;
   std::vector<cudaEvent_t> events;  // 2 per launch
@@ -45,6 +47,7 @@ gqa_status fail(gqa_status s, const char* fmt, ...) {
 }
 
 constexpr size_t kAlign = 256;
+constexpr long long kDefaultWaitBudget = 4000000000LL;   // clock cycles, about 2 s at the maximum SM clock
 constexpr long long kDecodeTargetCtas = 152LL * 16;  // GB300: 152 SMs, ~16 split CTAs per SM
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -290,6 +293,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   P.present_k = pk.data; P.present_v = pv.data;
   P.seqlens = static_cast<const int*>(in->seqlens_k.data);
   P.out = out->output.data;
+  P.wait_budget = hd->wait_budget;
+  P.withhold_tile = hd->withhold_tile;
 
   // ---- regime and workspace plan
   // A 4-bit cache is built by a prompt and always takes the prefill kernels, as
@@ -445,6 +450,8 @@ gqa_status gqa_create(const gqa_attrs* a, gqa_handle** out) {
   gqa_handle* h = new (std::nothrow) gqa_handle;
   if (!h) return fail(GQA_ERR_INVALID_ARGUMENT, "out of host memory");
   h->attrs = *a;
+  h->wait_budget = kDefaultWaitBudget;
+  h->withhold_tile = -1;
   h->profiling = false;
   h->used = 0;
   *out = h;
@@ -557,6 +564,16 @@ gqa_status gqa_forward_noalloc(gqa_handle* h, const gqa_inputs* in, const gqa_ou
   e = timed_launch(h, pl.tc_decode ? GQA_KERNEL_DECODE_TENSOR_CORE : GQA_KERNEL_DECODE, st,
                    [&] { return launch_decode_any(pl, st, maps); });
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return GQA_OK;
+}
+
+gqa_status gqa_set_wait_limit(gqa_handle* h, int64_t cycles, int32_t withhold_copy) {
+  if (!h) return fail(GQA_ERR_INVALID_ARGUMENT, "NULL handle");
+  if (cycles < 0 || (cycles > 0 && cycles < 1000))
+    return fail(GQA_ERR_INVALID_ARGUMENT, "wait limit must be 0 (default) or at least 1000 cycles");
+  if (withhold_copy < -1) return fail(GQA_ERR_INVALID_ARGUMENT, "withhold_copy must be -1 (off) or a tile index");
+  h->wait_budget = cycles == 0 ? kDefaultWaitBudget : (long long)cycles;
+  h->withhold_tile = withhold_copy;
   return GQA_OK;
 }
 

@@ -71,6 +71,9 @@ struct Params {
   int split_len;         // keys per decode split (tensor-core decode: keys per balanced unit)
   int max_splits;        // grid extent of the split axis (tensor-core decode: partial slots)
   int rows_pad;          // R: decode rows per (b, g) rounded to a power of two
+  // ---- bounded waits of the tensor-core kernels (gqa_set_wait_limit)
+  long long wait_budget; // clock cycles each pipeline wait may take before the CTA gives up
+  int withhold_tile;     // >= 0: the TMA warp stops before its copy of this key tile (tests the timeout path)
 };
 
 // Batch-level data check shared by all kernels: returns past_b (rows already

@@ -272,7 +272,7 @@ __device__ void transform_q_tiles(const Params& p, TcSmem& sm, int past, int r0,
         sn[k] = __ldg(reinterpret_cast<const uint4*>(sbase + cb));
       }
     }
-    if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_land[tile], 0)) && lane == 0) set_abort(p, sm);
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_land[tile], 0, p.wait_budget)) && lane == 0) set_abort(p, sm);
     uint8_t* qt = sm.q[tile];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -398,9 +398,10 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     __syncwarp();
     int issued = 0, issued_b = 0;
     for (int t = 0; t < ntiles; ++t) {
+      if (t == p.withhold_tile) break;   // testing: no copy of this tile, its waits expire
       const int st = t % kNS;
       const uint32_t ph = (uint32_t)(t / kNS) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[st], ph ^ 1u)) || aborted(sm)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[st], ph ^ 1u, p.wait_budget)) || aborted(sm)) {
         if (lane == 0) set_abort(p, sm);
         break;
       }
@@ -414,7 +415,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       __syncwarp();
       issued = t + 1;
       if constexpr (STAGED) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.bias_empty[st], ph ^ 1u)) || aborted(sm)) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.bias_empty[st], ph ^ 1u, p.wait_budget)) || aborted(sm)) {
           if (lane == 0) set_abort(p, sm);
           break;
         }
@@ -427,13 +428,13 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       }
     }
     // Drain: no copy of this CTA may still be landing when it exits.
-    mbar_wait(&sm.q_land[0], 0);
-    mbar_wait(&sm.q_land[1], 0);
+    mbar_wait(&sm.q_land[0], 0, p.wait_budget);
+    mbar_wait(&sm.q_land[1], 0, p.wait_budget);
     for (int t = max(0, issued_b - kNS); t < issued_b; ++t)
-      mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u);
+      mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u, p.wait_budget);
     for (int t = max(0, issued - kNS); t < issued; ++t) {
-      mbar_wait(&sm.k_full[t % kNS], (uint32_t)(t / kNS) & 1u);
-      mbar_wait(&sm.v_full[t % kNS], (uint32_t)(t / kNS) & 1u);
+      mbar_wait(&sm.k_full[t % kNS], (uint32_t)(t / kNS) & 1u, p.wait_budget);
+      mbar_wait(&sm.v_full[t % kNS], (uint32_t)(t / kNS) & 1u, p.wait_budget);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -468,14 +469,14 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     // Query tile t is ready once copied, or once rewritten in place when the
     // softmax threads apply norm / rotary; S_0(0) may start before tile 1 is.
     uint64_t* qready = qx ? sm.q_ready : sm.q_land;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&qready[0], 0) && mbar_wait(&sm.k_full[0], 0));
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&qready[0], 0, p.wait_budget) && mbar_wait(&sm.k_full[0], 0, p.wait_budget));
     if (ok) {
       if (elect_one()) {
         tc_fence_after();
         issue_s(0, 0);
       }
       __syncwarp();
-      ok = __all_sync(0xffffffffu, mbar_wait(&qready[1], 0));
+      ok = __all_sync(0xffffffffu, mbar_wait(&qready[1], 0, p.wait_budget));
     }
     if (ok) {
       if (elect_one()) {
@@ -487,7 +488,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
         const int st = t % kNS;
         const uint32_t ph = (uint32_t)(t / kNS) & 1u;
         const uint32_t tp = (uint32_t)t & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph, p.wait_budget))) {
           ok = false;
           break;
         }
@@ -501,7 +502,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           fence_async_smem();
         }
         __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[0], tp))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[0], tp, p.wait_budget))) {
           ok = false;
           break;
         }
@@ -512,13 +513,13 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
         __syncwarp();
         const bool more = t + 1 < ntiles;
         const int st1 = (t + 1) % kNS;
-        if (more && !__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st1], (uint32_t)((t + 1) / kNS) & 1u))) {
+        if (more && !__all_sync(0xffffffffu, mbar_wait(&sm.k_full[st1], (uint32_t)((t + 1) / kNS) & 1u, p.wait_budget))) {
           ok = false;
           break;
         }
         if (more && elect_one()) issue_s(0, st1);
         __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[1], tp))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[1], tp, p.wait_budget))) {
           ok = false;
           break;
         }
@@ -536,7 +537,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     // Drain: every MMA this thread issued has finished before tensor memory is freed.
     if (elect_one()) {
       mma_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0);
+      mbar_wait(&sm.drain, 0, p.wait_budget);
     }
     __syncwarp();
   } else {
@@ -567,8 +568,8 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     float m_run = kNegBig, l_run = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      bool got = mbar_wait(&sm.s_full[q], (uint32_t)t & 1u) && !aborted(sm);
-      if constexpr (STAGED) got = got && mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u);
+      bool got = mbar_wait(&sm.s_full[q], (uint32_t)t & 1u, p.wait_budget) && !aborted(sm);
+      if constexpr (STAGED) got = got && mbar_wait(&sm.bias_full[t % kNS], (uint32_t)(t / kNS) & 1u, p.wait_budget);
       if (!__all_sync(0xffffffffu, got)) {   // the warp leaves together
         ok = false;
         break;
@@ -814,7 +815,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       mbar_arrive(&sm.p_full[q]);
     }
     // ---- epilogue: O / l (+ sink), fp16, one row per thread
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(ntiles - 1) & 1u) && !aborted(sm));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(ntiles - 1) & 1u, p.wait_budget) && !aborted(sm));
     if (!ok) {
       set_abort(p, sm);
     } else {

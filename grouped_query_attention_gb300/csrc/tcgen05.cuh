@@ -43,9 +43,13 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Default bound of a pipeline wait, in clock cycles (about 2 s at the maximum
+// SM clock); a caller may ask for a shorter one (launch parameter).
+constexpr long long kDefaultWaitBudget = 4000000000LL;
+
 // Wait for the phase of the given parity to complete; false once `budget`
 // clock cycles have passed (the caller records a timeout and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget = 4000000000LL) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {

@@ -213,6 +213,23 @@ GQA_API gqa_status gqa_forward(gqa_handle* handle, const gqa_inputs* in, const g
 GQA_API gqa_status gqa_forward_noalloc(gqa_handle* handle, const gqa_inputs* in, const gqa_outputs* out,
                                        void* stream);
 
+/* Bound of the pipeline waits of the tensor-core kernels, for callers that
+ * want a data-dependent stall reported sooner, and a switch to test the
+ * timeout path (no counterpart on the operator's pages).
+ *   cycles: every barrier wait of a tensor-core CTA gives up after this many
+ *     SM clock cycles (0 restores the default, 4e9 cycles, about 2 s at the
+ *     maximum clock; otherwise at least 1000). A CTA whose wait gives up sets
+ *     GQA_DEVICE_TIMEOUT, stops its pipeline, waits for its own copies and
+ *     MMAs in flight, frees its tensor memory and returns; the call's outputs
+ *     are then undefined. The next call on the handle and workspace is
+ *     unaffected (each call clears the workspace header).
+ *   withhold_copy: -1 (default) off; k >= 0 makes the TMA warp of every
+ *     tensor-core CTA stop before the copy of its k-th key tile, so the waits
+ *     for that tile expire: a test of the timeout path that faults nothing.
+ * Applies to the following gqa_forward / gqa_forward_noalloc calls on the
+ * handle. Host-only; INVALID_ARGUMENT for a NULL handle or a value out of range. */
+GQA_API gqa_status gqa_set_wait_limit(gqa_handle* handle, int64_t cycles, int32_t withhold_copy);
+
 /* Synchronise `stream`, read and clear the status word that the kernels of
  * the most recent gqa_forward call on `workspace` set (each call clears it
  * first). *status receives the OR of GQA_DEVICE_* bits (0 = no data error).

@@ -340,3 +340,18 @@ def test_binding_constants_match_header():
     reg = dict(re.findall(r"#define (GQA_REGIME_\w+) (\d+)", header))
     for name, value in reg.items():
         assert getattr(capi, name) == int(value), name
+
+
+def test_set_wait_limit_argument_checks():
+    """gqa_set_wait_limit: 0 (default) or >= 1000 cycles, withhold_copy >= -1, a handle."""
+    lib = capi.load_library()
+    h = capi.gqa_create(capi.make_attrs(4, 2))
+    try:
+        assert lib.gqa_set_wait_limit(None, 0, -1) == capi.GQA_ERR_INVALID_ARGUMENT
+        assert lib.gqa_set_wait_limit(h, 999, -1) == capi.GQA_ERR_INVALID_ARGUMENT
+        assert lib.gqa_set_wait_limit(h, -5, -1) == capi.GQA_ERR_INVALID_ARGUMENT
+        assert lib.gqa_set_wait_limit(h, 2_000_000, -2) == capi.GQA_ERR_INVALID_ARGUMENT
+        assert lib.gqa_set_wait_limit(h, 2_000_000, 0) == capi.GQA_OK
+        assert lib.gqa_set_wait_limit(h, 0, -1) == capi.GQA_OK
+    finally:
+        capi.gqa_destroy(h)
