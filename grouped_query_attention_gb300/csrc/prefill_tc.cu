@@ -55,6 +55,7 @@ constexpr uint32_t kBox = 128u * 128u;          // one 64-column box of 128 rows
 constexpr uint32_t kTile = 2u * kBox;           // 128 rows x 128 columns = 32 KB
 constexpr float kLazy = 8.0f;                   // log2 growth tolerated before rescaling O
 constexpr uint32_t kIdS = idesc_f16(128, 128, 0, 0);   // Q (K-major) x K (K-major)
+constexpr uint32_t kIdS64 = idesc_f16(128, 64, 0, 0);  // Q x half a K tile (64 keys)
 constexpr uint32_t kIdO = idesc_f16(128, 128, 0, 1);   // P (tensor memory) x V (MN-major)
 
 struct __align__(1024) TcSmem {
@@ -67,6 +68,7 @@ struct __align__(1024) TcSmem {
   uint64_t k_full[kNS], v_full[kNS], kv_empty[kNS];
   uint64_t bias_full[kNS], bias_empty[kNS];
   uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t sb_full[2], sb_read[2];   // softcap / bias variants: second half of S landed / read (slab free)
   uint64_t drain;
   uint32_t tmem;
   int abort;
@@ -358,6 +360,8 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       mbar_init(&sm.s_full[q], 1);
       mbar_init(&sm.p_full[q], kBM);
       mbar_init(&sm.o_done[q], 1);
+      mbar_init(&sm.sb_full[q], 1);
+      mbar_init(&sm.sb_read[q], 4);   // one arrival per softmax warp of the group
     }
     if constexpr (STAGED) {
       for (int s = 0; s < kNS; ++s) {
@@ -466,42 +470,70 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       for (int ks = 0; ks < 8; ++ks) mma_f16_ts(d, pa + ks * 8, b0 + (uint64_t)(ks * 128), kIdO, acc || ks > 0);
       mma_commit(&sm.o_done[q]);
     };
+    // Softcap / bias variants: S in two halves of 64 keys (N = 64) in the two
+    // 64-column slabs of the group's tensor memory. Tile t: keys 0..63 in slab
+    // t & 1 (A), keys 64..127 in the other (B); P of the whole tile is packed
+    // into slab A. So slab B is free as soon as the softmax has read the second
+    // half, and the first half of S(t+1) goes there while the softmax finishes
+    // tile t; the second half follows P.V(t) into slab A.
+    auto issue_s_half = [&](int q, int st, int half, int slab) {
+      const uint32_t d = tmem + q * 128 + slab * 64;
+      const uint64_t a0 = dq[q], b0 = dk0 + (uint64_t)(st * (int)(kTile >> 4) + half * 512);   // 64 key rows = 8 KB
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t off = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
+        mma_f16_ss(d, a0 + off, b0 + off, kIdS64, ks > 0);
+      }
+      mma_commit(half == 0 ? &sm.s_full[q] : &sm.sb_full[q]);
+    };
+    auto issue_pv_slab = [&](int q, int st, bool acc, int slab) {
+      const uint32_t d = tmem + 256 + q * 128;
+      const uint32_t pa = tmem + q * 128 + slab * 64;   // P packed over slab A of the tile
+      const uint64_t b0 = dv0 + (uint64_t)(st * (int)(kTile >> 4));
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) mma_f16_ts(d, pa + ks * 8, b0 + (uint64_t)(ks * 128), kIdO, acc || ks > 0);
+      mma_commit(&sm.o_done[q]);
+    };
+    // V rows past the key range (stale cache rows may hold any bits) are zeroed.
+    auto wait_v = [&](int t, int st) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], (uint32_t)(t / kNS) & 1u, p.wait_budget))) return false;
+      const int valid = kmax - (kmin + t * kBN);
+      if (valid < kBN) {
+        for (int x = lane; x < (kBN - valid) * 16; x += 32) {
+          const int r = valid + x / 16, c = x % 16;
+          *reinterpret_cast<uint4*>(sm.v[st] + (c >> 3) * kBox + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_async_smem();
+      }
+      __syncwarp();
+      return true;
+    };
     // Query tile t is ready once copied, or once rewritten in place when the
     // softmax threads apply norm / rotary; S_0(0) may start before tile 1 is.
     uint64_t* qready = qx ? sm.q_ready : sm.q_land;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&qready[0], 0, p.wait_budget) && mbar_wait(&sm.k_full[0], 0, p.wait_budget));
-    if (ok) {
+    for (int q = 0; q < 2 && ok; ++q) {
+      if (q == 1) ok = __all_sync(0xffffffffu, mbar_wait(&qready[1], 0, p.wait_budget));
+      if (!ok) break;
       if (elect_one()) {
         tc_fence_after();
-        issue_s(0, 0);
+        if constexpr (PLAIN) {
+          issue_s(q, 0);
+        } else {
+          issue_s_half(q, 0, 0, 0);
+          issue_s_half(q, 0, 1, 1);
+        }
       }
       __syncwarp();
-      ok = __all_sync(0xffffffffu, mbar_wait(&qready[1], 0, p.wait_budget));
     }
-    if (ok) {
-      if (elect_one()) {
-        tc_fence_after();
-        issue_s(1, 0);
-      }
-      __syncwarp();
+    if constexpr (PLAIN) {
       for (int t = 0; t < ntiles && ok; ++t) {
         const int st = t % kNS;
-        const uint32_t ph = (uint32_t)(t / kNS) & 1u;
         const uint32_t tp = (uint32_t)t & 1u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&sm.v_full[st], ph, p.wait_budget))) {
+        if (!wait_v(t, st)) {
           ok = false;
           break;
         }
-        // Zero V rows past the key range (stale cache rows may hold any bits).
-        const int valid = kmax - (kmin + t * kBN);
-        if (valid < kBN) {
-          for (int x = lane; x < (kBN - valid) * 16; x += 32) {
-            const int r = valid + x / 16, c = x % 16;
-            *reinterpret_cast<uint4*>(sm.v[st] + (c >> 3) * kBox + r * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          fence_async_smem();
-        }
-        __syncwarp();
         if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[0], tp, p.wait_budget))) {
           ok = false;
           break;
@@ -530,6 +562,42 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           if (more) issue_s(1, st1);
         }
         __syncwarp();
+        if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
+      }
+    } else {
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const int st = t % kNS, slab_a = t & 1, slab_b = slab_a ^ 1;
+        const uint32_t tp = (uint32_t)t & 1u;
+        const bool more = t + 1 < ntiles;
+        const int st1 = (t + 1) % kNS;
+        for (int q = 0; q < 2 && ok; ++q) {
+          // S_q(t+1), keys 0..63: slab B once the softmax has read the second half of S_q(t).
+          if (more) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.sb_read[q], tp, p.wait_budget) &&
+                                             mbar_wait(&sm.k_full[st1], (uint32_t)((t + 1) / kNS) & 1u, p.wait_budget))) {
+              ok = false;
+              break;
+            }
+            if (elect_one()) {
+              tc_fence_after();
+              issue_s_half(q, st1, 0, slab_b);
+            }
+            __syncwarp();
+          }
+          if ((q == 0 && !wait_v(t, st)) ||
+              !__all_sync(0xffffffffu, mbar_wait(&sm.p_full[q], tp, p.wait_budget))) {
+            ok = false;
+            break;
+          }
+          // P.V(t) reads P from slab A; S_q(t+1), keys 64..127, then overwrites it.
+          if (elect_one()) {
+            tc_fence_after();
+            issue_pv_slab(q, st, t > 0, slab_a);
+            if (q == 1) mma_commit(&sm.kv_empty[st]);
+            if (more) issue_s_half(q, st1, 1, slab_a);
+          }
+          __syncwarp();
+        }
         if (__any_sync(0xffffffffu, aborted(sm))) ok = false;
       }
     }
@@ -652,11 +720,21 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           tmem_st32(s_addr + hf * 32, packed);
         }
       } else {
+        // Keys 0..63 of the tile in slab A = t & 1, keys 64..127 in slab B (the
+        // other one, landing later); P of both halves is packed into slab A.
+        const uint32_t s_a = s_addr + (uint32_t)(t & 1) * 64, s_b = s_addr + (uint32_t)((t & 1) ^ 1) * 64;
+        bool half_ok = true;
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t s_h = hf == 0 ? s_a : s_b;
+          if (hf == 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.sb_full[q], (uint32_t)t & 1u, p.wait_budget))) {
+            half_ok = false;
+            break;
+          }
+          tc_fence_after();
           uint32_t r[64];
-          tmem_ld32(s_addr + hf * 64, r);
-          tmem_ld32(s_addr + hf * 64 + 32, r + 32);
+          tmem_ld32(s_h, r);
+          tmem_ld32(s_h + 32, r + 32);
           tmem_ld_wait();
           // Transform the half in place: scale, softcap, bias. With a softcap the
           // FMA-pipe polynomial goes first and is checked afterwards (|u| <= 1/4
@@ -731,13 +809,18 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           if constexpr (CAP) {
             const float zmax = transform(true);
             if (__any_sync(0xffffffffu, !(zmax <= kc.y3))) {
-              tmem_ld32(s_addr + hf * 64, r);
-              tmem_ld32(s_addr + hf * 64 + 32, r + 32);
+              tmem_ld32(s_h, r);
+              tmem_ld32(s_h + 32, r + 32);
               tmem_ld_wait();
               transform(false);
             }
           } else {
             transform(false);
+          }
+          if (hf == 1) {   // slab B read: the MMA may put the next tile's first half there
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sb_read[q]);
           }
           if (!full) {   // warp-uniform: only tiles on a mask boundary pay for the selects
 #pragma unroll
@@ -756,7 +839,12 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             const float m_new = grow ? mh : m_run;
             const float f = grow ? ex2(m_run - m_new) : 1.0f;
             if (t > 0) {
-              // O_q is complete up to tile t-1 (its MMAs precede S_q(t)): rescale it in place.
+              // Rescale O_q in place once it holds P.V up to tile t-1: the first
+              // half of S_q(t) is issued before P.V(t-1), so that half waits for
+              // it; the second half of S_q(t) is issued after it.
+              if (hf == 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(t - 1) & 1u, p.wait_budget)))
+                half_ok = false;
+              tc_fence_after();
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 uint32_t raw[32];
@@ -771,7 +859,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
               // P of the first half was written with the old reference.
               uint32_t pk[32];
               tmem_st_wait();
-              tmem_ld32(s_addr, pk);
+              tmem_ld32(s_a, pk);
               tmem_ld_wait();
               const float2 f2 = make_float2(f, f);
 #pragma unroll
@@ -781,7 +869,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
                 const __half2 hw = __floats2half2_rn(w.x, w.y);
                 pk[k] = *reinterpret_cast<const uint32_t*>(&hw);
               }
-              tmem_st32(s_addr, pk);
+              tmem_st32(s_a, pk);
             }
             l_run *= f;
             ls2.x *= f;
@@ -800,7 +888,11 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             const __half2 hp = __floats2half2_rn(pa, pb);
             packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
           }
-          tmem_st32(s_addr + hf * 32, packed);
+          tmem_st32(s_a + hf * 32, packed);
+        }
+        if (!half_ok) {
+          ok = false;
+          break;
         }
         if constexpr (STAGED) {
           // The warp's bias reads have returned (their values are used above).
