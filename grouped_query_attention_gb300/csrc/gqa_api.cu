@@ -73,7 +73,8 @@ std::string shape_str(const gqa_tensor& t) {
 struct Plan {
   gqa::Params P;
   bool decode;
-  bool tensor_core;  // prefill on the tcgen05 kernel (fp16, head size 128)
+  bool tensor_core;  // prefill on a tcgen05 kernel (head size 128)
+  bool tcq;          // ... the one over an int8 / 4-bit cache with fp32 Q/K/V
   bool tc_decode;    // decode on a tcgen05 kernel (fp16 cache <= 16 rows, or int8 cache with fp32 <= 8 rows; H=128)
   bool tc_i8;        // ... the int8-cache one
   size_t hdr_bytes, qprep_bytes, kvsep_bytes, bias_bytes, part_bytes, total_bytes;
@@ -307,6 +308,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   pl->tc_i8 = pl->decode && gqa::decode_tc_i8_supported(P);
   pl->tc_decode = pl->decode && (gqa::decode_tc_supported(P) || pl->tc_i8);
   pl->tensor_core = false;
+  pl->tcq = false;
   pl->hdr_bytes = align_up(sizeof(unsigned int) * (1 + (size_t)B * Nkv));  // status, tickets
   pl->qprep_bytes = 0;
   pl->kvsep_bytes = 0;
@@ -339,7 +341,8 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
   } else {
     if (!gqa::prefill_simt_supported(P) || !gqa::prepass_supported(P))
       return fail(GQA_ERR_UNSUPPORTED, "no prefill kernel for head_size %lld", H);
-    pl->tensor_core = !window && gqa::prefill_tc_supported(P);
+    pl->tcq = !window && gqa::prefill_tcq_supported(P);
+    pl->tensor_core = !window && (gqa::prefill_tc_supported(P) || pl->tcq);
     // The tensor-core prefill loads the raw query rows of a tile (when the
     // group size divides its 128 rows) and applies norm / rotary itself;
     // otherwise the pre-pass prepares fp16 queries for it, and fp32 ones for
@@ -348,7 +351,7 @@ gqa_status plan_call(const gqa_handle* hd, const gqa_inputs* in, const gqa_outpu
     P.qprep_type = pl->tensor_core ? gqa::kF16 : gqa::kF32;
     pl->qprep_bytes = P.q_in_prefill ? 0 : align_up((size_t)B * S * N * H * (pl->tensor_core ? 2 : 4));
     if (separate) pl->kvsep_bytes = 2 * align_up((size_t)B * Nkv * S * H * (tdt == GQA_F16 ? 2 : 4));
-    if (pl->tensor_core && gqa::prefill_tc_bias_staged(P)) {
+    if (pl->tensor_core && !pl->tcq && gqa::prefill_tc_bias_staged(P)) {
       pl->bias_staged = true;
       P.bias_stage_ld = (int)((P.bias_ld + 3) & ~3);   // 16-byte rows for the tensor copies
       pl->bias_bytes = align_up((size_t)P.bias_bdim * S * P.bias_stage_ld * sizeof(float));
@@ -503,7 +506,7 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
   if (pl.decode && pl.tc_decode)
     e = pl.tc_i8 ? gqa::prepare_decode_tc_i8(P, &maps) : gqa::prepare_decode_tc(P, &maps);
   else if (!pl.decode && pl.tensor_core)
-    e = gqa::prepare_prefill_tc(P, &maps);
+    e = pl.tcq ? gqa::prepare_prefill_tcq(P, &maps) : gqa::prepare_prefill_tc(P, &maps);
   if (e != cudaSuccess) return cuda_fail(e, "TMA tensor maps");
   if (P.window_cache) {
     e = timed_launch(h, GQA_KERNEL_WINDOW_SHIFT, st, [&] { return gqa::launch_window_shift(P, st); });
@@ -524,7 +527,9 @@ gqa_status gqa_forward(gqa_handle* h, const gqa_inputs* in, const gqa_outputs* o
       if (e != cudaSuccess) return cuda_fail(e, "bias staging launch");
     }
     if (pl.tensor_core)
-      e = timed_launch(h, GQA_KERNEL_PREFILL_TENSOR_CORE, st, [&] { return gqa::launch_prefill_tc(P, st, maps); });
+      e = timed_launch(h, GQA_KERNEL_PREFILL_TENSOR_CORE, st, [&] {
+        return pl.tcq ? gqa::launch_prefill_tcq(P, st, maps) : gqa::launch_prefill_tc(P, st, maps);
+      });
     else
       e = timed_launch(h, GQA_KERNEL_PREFILL_CUDA_CORE, st, [&] { return gqa::launch_prefill_simt(P, st); });
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -153,6 +153,10 @@ cudaError_t launch_prefill_simt(const Params& p, cudaStream_t st);
 cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps);
 cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& maps);
 bool prefill_tc_supported(const Params& p);
+// Tensor-core prefill over an int8 / 4-bit cache with fp32 Q/K/V (hi/lo fp16 split).
+bool prefill_tcq_supported(const Params& p);
+cudaError_t prepare_prefill_tcq(const Params& p, TmaMaps* maps);
+cudaError_t launch_prefill_tcq(const Params& p, cudaStream_t st, const TmaMaps& maps);
 bool decode_supported(const Params& p);
 bool prepass_supported(const Params& p);
 bool prefill_simt_supported(const Params& p);

@@ -22,8 +22,21 @@ cudaError_t encode_fp16_2d_sw128(CUtensorMap* map, const void* base, uint64_t ro
 cudaError_t encode_fp16_query_sw128(CUtensorMap* map, const void* base, uint64_t B, uint64_t S, uint64_t N,
                                     uint32_t G);
 
-// The same for a row-major [rows][cols] matrix of bytes (int8 codes): boxes of
-// box_cols (<= 128) x box_rows bytes with the 128-byte swizzle.
+// 4D map of a (B, S, N, 128) fp32 query tensor with the 128-byte swizzle:
+// boxes of 32 dims x G heads x 128/G positions x 1 batch land as 128 rows of
+// 128 bytes in (position, head) order; positions past S read as zero. G must
+// divide 128.
+cudaError_t encode_f32_query_sw128(CUtensorMap* map, const void* base, uint64_t B, uint64_t S, uint64_t N,
+                                   uint32_t G);
+
+// 2D map of a row-major [rows][cols] byte matrix without swizzle: boxes of
+// box_cols (a multiple of 16, <= 256) x box_rows bytes land as box_rows dense
+// rows; rows past the matrix read as zero.
+cudaError_t encode_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride_bytes,
+                         uint32_t box_cols, uint32_t box_rows);
+
+// 2D map of a row-major [rows][cols] byte matrix (int8 codes) with the
+// 128-byte swizzle: boxes of box_cols (<= 128) x box_rows bytes.
 cudaError_t encode_u8_2d_sw128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                                uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
 

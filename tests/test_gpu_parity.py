@@ -166,6 +166,27 @@ PREFILL = {
     "i4_bidirectional_softcap_sink": spec(dtype="f32", N=4, Nkv=2, S=33, mode="prompt", capacity=33, causal=0,
                                           seqlens_k=(32, 20, 5), seqlens_range=None, quant="PER_TENSOR", bits=4,
                                           softcap=20.0, head_sink=True, scale_range=(0.2, 0.3)),
+    # tensor-core prefill over int8 / 4-bit caches with fp32 Q/K/V (hi/lo fp16 split): several
+    # query-tile pairs and key tiles, ragged tails, group sizes 1 and 8, every feature
+    "i8_tcq_multi_tile_g8_norm_rotary": spec(dtype="f32", B=2, S=300, N=16, Nkv=2, capacity=2500,
+                                             seqlens_range=(300, 2400), quant="PER_CHANNEL", qk_norm=True,
+                                             rotary_theta=1e4, scale_range=(0.01, 0.05)),
+    "i4_tcq_bidirectional_g1_prompt_padding": spec(dtype="f32", S=150, N=2, Nkv=2, mode="prompt", capacity=160,
+                                                   seqlens_k=(149, 70, 3), seqlens_range=None, causal=0,
+                                                   quant="PER_TENSOR", bits=4, scale_range=(0.2, 0.3)),
+    "i8_tcq_copy_smooth_window": spec(dtype="f32", S=12, N=8, Nkv=2, mode="copy", past_len=300,
+                                      seqlens_range=(11, 311), local_window_size=100, smooth_softmax=1,
+                                      quant="PER_TENSOR", scale_range=(0.01, 0.03)),
+    "i8_tcq_bias_large_spread_softcap": spec(dtype="f32", S=64, N=16, Nkv=2, softcap=30.0, bias=(1, 1, 8.0),
+                                             head_sink=True, seqlens_range=(64, 600), quant="PER_CHANNEL",
+                                             scale_range=(0.01, 0.05)),
+    "i8_tcq_per_head_bias_small_softcap": spec(dtype="f32", S=40, N=4, Nkv=2, softcap=1.0, bias=(3, 4, 2.0),
+                                               seqlens_range=(40, 500), quant="PER_CHANNEL",
+                                               scale_range=(0.01, 0.05)),
+    "i4_tcq_prompt_g4_norm_rotary_window": spec(dtype="f32", B=2, S=700, N=16, Nkv=4, mode="prompt",
+                                                capacity=700, seqlens_k=(699, 400), seqlens_range=None,
+                                                quant="PER_CHANNEL", bits=4, qk_norm=True, rotary_theta=1e4,
+                                                local_window_size=300, scale_range=(0.15, 0.4)),
     "i4_h256_window_generic_prepass": spec(dtype="f32", H=256, N=4, Nkv=2, S=20, mode="prompt", capacity=24,
                                            seqlens_k=(19, 19, 10), seqlens_range=None, quant="PER_CHANNEL", bits=4,
                                            local_window_size=5, scale_range=(0.1, 0.3)),
