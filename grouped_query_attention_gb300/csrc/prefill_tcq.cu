@@ -16,21 +16,22 @@
 // CTA = two 128-row query tiles of one KV head (b, g), rows = (position,
 // grouped head) as in the fp16 prefill. Warp roles (384 threads):
 //   warp 0       TMA: the raw fp32 query rows of both tiles (four boxes of 32
-//                dimensions, 128-byte swizzle), then the code tiles of K and V
-//                (one staging buffer each, no swizzle).
+//                dimensions, 128-byte swizzle).
 //   warp 1       MMA issue and tensor-memory allocation.
-//   warps 2..9   softmax, one thread per row of query tile (warp - 2) / 4;
-//                before the loop each thread rewrites its own query row in
-//                place as the hi and lo fp16 operand rows (the 128-byte lines
-//                of a row are the same before and after, so no thread touches
-//                another's bytes).
-//   warps 10,11  converters: code tile -> fp16 operand tile (K-major K,
-//                MN-major V, 128-byte swizzle), 64 key rows each.
-// Shared memory: query tiles 128 KB, one fp16 K and one fp16 V operand tile
-// (64 KB), one code tile each (32 KB). Tensor memory: S0 | S1 | O0 | O1.
-// The MMA order is the fp16 prefill's (P.V of one tile, then S of the other
-// tile's next key tile), so the converters write K(t+1) while P_0.V(t) runs
-// and V(t) while S_1(t) runs. Every barrier wait is bounded.
+//   warps 2..9   all eight first rewrite the two query tiles in place as the
+//                hi and lo fp16 operand tiles (8 lanes per row); then softmax,
+//                one thread per row of query tile (warp - 2) / 4, and the
+//                epilogue, which stages O in the group's query region and
+//                writes it with tensor stores.
+//   warps 10..13 converters, 32 key rows each: the codes of the next K or V
+//                tile are loaded from global memory into registers while the
+//                current one is converted to its fp16 operand tile (K-major
+//                K, two buffers; MN-major V, one buffer; 128-byte swizzle).
+// Shared memory: query tiles 128 KB, fp16 K 2 x 32 KB, fp16 V 32 KB.
+// Tensor memory: S0 | S1 | O0 | O1. The MMA order is the fp16 prefill's (P.V
+// of one tile, then S of the other tile's next key tile); K(t+1) may be
+// converted from the moment S_1(t-1) is done, V(t) while S_1(t) runs. Every
+// barrier wait is bounded.
 //
 // com.microsoft.GroupQueryAttention, section Implementation variants
 // (quant_int8_flash_prefill, quant_int4_flash_prefill: attention over the
@@ -50,8 +51,10 @@ using namespace tc;
 constexpr int kBM = 128;                       // rows per query tile
 constexpr int kBN = 128;                       // keys per K/V tile
 constexpr int kHD = 128;                       // head size
-constexpr int kThreads = 384;
+constexpr int kThreads = 448;
 constexpr int kConvWarp0 = 10;                 // first converter warp
+constexpr int kConvWarps = 4;                  // converter warps, 32 key rows each
+constexpr int kConvRows = kBN / kConvWarps;
 constexpr uint32_t kBox = 128u * 128u;         // 128 rows x 128 bytes = 16 KB
 constexpr uint32_t kTile = 2u * kBox;          // fp16 operand tile, 128 x 128
 constexpr uint32_t kQRegion = 4u * kBox;       // fp32 query tile = hi and lo fp16 tiles
@@ -62,15 +65,14 @@ constexpr uint32_t kIdO = idesc_f16(128, 128, 0, 1);   // P (tensor memory) x V 
 struct __align__(1024) QcSmem {
   // Per query tile: box k holds dims 32k .. 32k+31 (fp32) as copied; after the
   // rewrite boxes 0, 1 are the hi fp16 tile (dims 0..63, 64..127) and boxes
-  // 2, 3 the lo fp16 tile.
+  // 2, 3 the lo fp16 tile; after the last S MMA the epilogue stages O here
+  // (fp32, the copied layout).
   uint8_t q[2][kQRegion];
-  uint8_t kf[kTile];            // K codes as fp16, K-major (the B operand of S)
+  uint8_t kf[2][kTile];         // K codes as fp16, K-major (the B operand of S), tile t in buffer t & 1
   uint8_t vf[kTile];            // V codes as fp16, MN-major (the B operand of O)
-  uint8_t kc[kBox];             // K code tile as copied: 128 rows of 128 (int8) or 64 (4-bit) bytes
-  uint8_t vc[kBox];
+  float rho[2][kBM];            // 2^e of each query row (S 2^e is the scaled score)
   uint64_t q_land[2], q_ready[2];
-  uint64_t kc_full, kc_empty, vc_full, vc_empty;   // code tiles: copy -> converters
-  uint64_t kf_full, kf_empty, vf_full, vf_empty;   // fp16 tiles: converters -> MMA
+  uint64_t kf_full[2], kf_empty[2], vf_full, vf_empty;   // fp16 tiles: converters <-> MMA
   uint64_t s_full[2], p_full[2], o_done[2];
   uint64_t drain;
   uint32_t tmem;
@@ -125,142 +127,186 @@ __device__ __forceinline__ void i4x32_to_h32(uint4 w, uint32_t* h) {
   }
 }
 
-// Rows [row0, row0 + 64) of a code tile `src` into the fp16 operand tile
-// `dst` (128-byte swizzle; box bx = dims 64 bx .. 64 bx + 63). One warp;
-// every lane handles one 16-byte chunk of codes per step, four steps of
-// loads in flight.
+// Codes of key rows [row0, row0 + 32) of a tile whose first cache row is
+// `grow0`: lane l takes 16-byte chunk x = 32 s + l of the 32-row block in step
+// s (row x / chunks, chunk x % chunks); rows past the cache read as zeros.
 template <int BITS>
-__device__ __forceinline__ void convert_rows(const uint8_t* src, uint8_t* dst, int row0, int lane) {
-  constexpr int kRowBytes = BITS == 8 ? 128 : 64;       // code bytes per row
-  constexpr int kChunks = kRowBytes / 16;               // code chunks per row
-  constexpr int kSteps = 64 * kChunks / 32;             // chunks per lane
+__device__ __forceinline__ void load_codes(const uint8_t* cache, long long grow0, long long nrows_cache, int row0,
+                                           int lane, uint4* w) {
+  constexpr int kRowBytes = BITS == 8 ? 128 : 64;
+  constexpr int kChunks = kRowBytes / 16;
+  constexpr int kSteps = kConvRows * kChunks / 32;
 #pragma unroll
-  for (int s0 = 0; s0 < kSteps; s0 += 4) {
-    uint4 w[4];
+  for (int s = 0; s < kSteps; ++s) {
+    const int x = s * 32 + lane, row = row0 + x / kChunks, j = x % kChunks;
+    const long long gr = grow0 + row;
+    w[s] = gr < nrows_cache ? __ldg(reinterpret_cast<const uint4*>(cache + gr * kRowBytes + j * 16))
+                            : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The codes of load_codes as fp16 into the operand tile `dst` (128-byte
+// swizzle; box bx = dims 64 bx .. 64 bx + 63).
+template <int BITS>
+__device__ __forceinline__ void store_codes_h(const uint4* w, uint8_t* dst, int row0, int lane) {
+  constexpr int kRowBytes = BITS == 8 ? 128 : 64;
+  constexpr int kChunks = kRowBytes / 16;
+  constexpr int kSteps = kConvRows * kChunks / 32;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int x = (s0 + k) * 32 + lane, row = row0 + x / kChunks, j = x % kChunks;
-      w[k] = *reinterpret_cast<const uint4*>(src + row * kRowBytes + j * 16);
-    }
+  for (int s = 0; s < kSteps; ++s) {
+    const int x = s * 32 + lane, row = row0 + x / kChunks, j = x % kChunks;
+    if constexpr (BITS == 8) {
+      // chunk j: dims 16 j .. 16 j + 15 = fp16 chunks 2 (j % 4), +1 of box j / 4
+      uint32_t h[8];
+      i8x16_to_h16(w[s], h);
+      uint8_t* b = dst + (j >> 2) * kBox;
+      *reinterpret_cast<uint4*>(b + sw128_offset(row, 2 * (j & 3))) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(b + sw128_offset(row, 2 * (j & 3) + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+    } else {
+      // chunk j: dims 32 j .. 32 j + 31 = fp16 chunks 4 (j % 2) .. +3 of box j / 2
+      uint32_t h[16];
+      i4x32_to_h32(w[s], h);
+      uint8_t* b = dst + (j >> 1) * kBox;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int x = (s0 + k) * 32 + lane, row = row0 + x / kChunks, j = x % kChunks;
-      if constexpr (BITS == 8) {
-        // chunk j: dims 16 j .. 16 j + 15 = fp16 chunks 2 (j % 4), +1 of box j / 4
-        uint32_t h[8];
-        i8x16_to_h16(w[k], h);
-        uint8_t* b = dst + (j >> 2) * kBox;
-        *reinterpret_cast<uint4*>(b + sw128_offset(row, 2 * (j & 3))) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(b + sw128_offset(row, 2 * (j & 3) + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-      } else {
-        // chunk j: dims 32 j .. 32 j + 31 = fp16 chunks 4 (j % 2) .. +3 of box j / 2
-        uint32_t h[16];
-        i4x32_to_h32(w[k], h);
-        uint8_t* b = dst + (j >> 1) * kBox;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(b + sw128_offset(row, 4 * (j & 1) + c)) =
-              make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-      }
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(b + sw128_offset(row, 4 * (j & 1) + c)) =
+            make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
     }
   }
 }
 
-// One query row, in place: the thread of row rl reads the row's 128 fp32
-// values (box k, chunk c: dims 32 k + 4 c ..), applies RMS norm (weights
-// q_norm_weight), rotary at absolute position `pos` (first half / second half
-// pairs, cos/sin_cache rows), the score scale and the K channel scale, and
-// writes hi and lo fp16 rows over the same four 128-byte lines (hi: boxes 0,
-// 1; lo: boxes 2, 3). Returns 2^e, the factor that brings S = (hi + lo) .
-// codes back to the scaled score. Queries feed only the scores, so the
-// rounding order is free (fused multiply-adds). Rows of the tile past the
-// block were filled with zeros by the copy and stay zero.
-__device__ float split_query_row(const Params& p, uint8_t* qt, int rl, int g, int pos, float qscale) {
-  float x[kHD];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float4 v = *reinterpret_cast<const float4*>(qt + k * kBox + sw128_offset(rl, c));
-      x[32 * k + 4 * c] = v.x;
-      x[32 * k + 4 * c + 1] = v.y;
-      x[32 * k + 4 * c + 2] = v.z;
-      x[32 * k + 4 * c + 3] = v.w;
-    }
-  }
+// All bits of `v` over the 128 threads of softmax group q (named barrier 1 + q).
+__device__ __forceinline__ bool group_all(bool v, int q) {
+  uint32_t r;
+  asm volatile("{ .reg .pred p, c; setp.ne.u32 c, %1, 0; bar.red.and.pred p, %2, 128, c; selp.u32 %0, 1, 0, p; }"
+               : "=r"(r)
+               : "r"((uint32_t)v), "r"(1 + q)
+               : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void ld_f8(const float* src, float* f) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void lds_f8(const uint8_t* line, int c0, int rl, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(line + sw128_offset(rl, c0));
+  const float4 b = *reinterpret_cast<const float4*>(line + sw128_offset(rl, c0 + 1));
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Both query tiles, in place, by the 256 softmax threads (wt = 0..255): 8
+// lanes per row (lane l8: dims 8 l8 .. and 64 + 8 l8 .., so the rotary
+// partner is in the lane), 32 rows per pass, four passes per tile. A row is
+// normalised (q_norm_weight), rotated at its absolute position (cos/sin_cache),
+// scaled (score scale, K channel scale), brought to [1, 2) by 2^-e and split
+// into hi = fp16(x) and lo = fp16(x - hi), written over the same four 128-byte
+// lines that held it (hi: boxes 0, 1; lo: boxes 2, 3); 2^e goes to rho. The
+// lanes of a row read before any of them writes (__syncwarp). Queries feed
+// only the scores, so the rounding order is free (fused multiply-adds).
+// Rows past the block were filled with zeros by the copy and stay zero.
+__device__ void split_query_tiles(const Params& p, QcSmem& sm, int past, int r0, int nrows, int g, int wt,
+                                  float qscale) {
+  const int l8 = wt & 7, sub = wt >> 3, lane = wt & 31;
+  float wlo[8], whi[8], klo[8], khi[8];
   if (p.has_norm) {
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int d = 0; d < kHD; ++d) s4[d & 3] = fmaf(x[d], x[d], s4[d & 3]);
-    const float rn = rsqrtf((s4[0] + s4[1] + s4[2] + s4[3]) * (1.0f / kHD) + p.eps);
-    const float4* w4 = reinterpret_cast<const float4*>(p.qw);
-#pragma unroll
-    for (int d4 = 0; d4 < kHD / 4; ++d4) {
-      const float4 w = __ldg(w4 + d4);
-      x[4 * d4] *= rn * w.x;
-      x[4 * d4 + 1] *= rn * w.y;
-      x[4 * d4 + 2] *= rn * w.z;
-      x[4 * d4 + 3] *= rn * w.w;
-    }
+    ld_f8(reinterpret_cast<const float*>(p.qw) + 8 * l8, wlo);
+    ld_f8(reinterpret_cast<const float*>(p.qw) + 64 + 8 * l8, whi);
   }
-  if (p.has_rotary) {
-    const float4* c4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.cos_c) + (long long)pos * (kHD / 2));
-    const float4* s4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.sin_c) + (long long)pos * (kHD / 2));
-#pragma unroll
-    for (int d4 = 0; d4 < kHD / 8; ++d4) {
-      const float4 c = __ldg(c4 + d4), s = __ldg(s4 + d4);
-      const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = 4 * d4 + e;
-        const float a = x[d], b = x[d + kHD / 2];
-        x[d] = fmaf(a, cc[e], -b * ss[e]);
-        x[d + kHD / 2] = fmaf(b, cc[e], a * ss[e]);
-      }
-    }
-  }
-  float mx = 0.f;
   if (p.k_scale_n == 1) {
-    const float ks = qscale * p.k_scale[0];
 #pragma unroll
-    for (int d = 0; d < kHD; ++d) {
-      x[d] *= ks;
-      mx = fmaxf(mx, fabsf(x[d]));
-    }
+    for (int k = 0; k < 8; ++k) klo[k] = khi[k] = qscale * p.k_scale[0];
   } else {
-    const float4* k4 = reinterpret_cast<const float4*>(p.k_scale + (long long)g * kHD);
+    ld_f8(p.k_scale + g * kHD + 8 * l8, klo);
+    ld_f8(p.k_scale + g * kHD + 64 + 8 * l8, khi);
 #pragma unroll
-    for (int d4 = 0; d4 < kHD / 4; ++d4) {
-      const float4 s = __ldg(k4 + d4);
-      x[4 * d4] *= qscale * s.x;
-      x[4 * d4 + 1] *= qscale * s.y;
-      x[4 * d4 + 2] *= qscale * s.z;
-      x[4 * d4 + 3] *= qscale * s.w;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(x[4 * d4 + e]));
+    for (int k = 0; k < 8; ++k) {
+      klo[k] *= qscale;
+      khi[k] *= qscale;
     }
   }
-  // 2^e <= mx < 2^(e+1) from the exponent bits (mx = 0 or subnormal: e = 0).
-  const int ebits = (__float_as_int(mx) >> 23) & 0xff;
-  const int e = ebits == 0 ? 0 : ebits - 127;
-  const float down = __int_as_float((127 - e) << 23), up = __int_as_float((127 + e) << 23);
-#pragma unroll
-  for (int c16 = 0; c16 < kHD / 8; ++c16) {   // fp16 chunk: dims 8 c16 .. 8 c16 + 7
-    uint32_t hw[4], lw[4];
-#pragma unroll
+  const float* cbase = reinterpret_cast<const float*>(p.cos_c);
+  const float* sbase = reinterpret_cast<const float*>(p.sin_c);
+  for (int tile = 0; tile < 2; ++tile) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.q_land[tile], 0, p.wait_budget)) && lane == 0) set_abort(p, sm);
+    uint8_t* qt = sm.q[tile];
+#pragma unroll 1
     for (int k = 0; k < 4; ++k) {
-      const float a = x[8 * c16 + 2 * k] * down, b = x[8 * c16 + 2 * k + 1] * down;
-      const __half2 h = __floats2half2_rn(a, b);
-      const float2 hf = __half22float2(h);
-      const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-      hw[k] = *reinterpret_cast<const uint32_t*>(&h);
-      lw[k] = *reinterpret_cast<const uint32_t*>(&l);
+      const int rl = k * 32 + sub;                               // row inside the tile
+      const int r = min(r0 + tile * kBM + rl, nrows - 1);
+      float lo[8], hi[8];
+      lds_f8(qt + (l8 >> 2) * kBox, 2 * (l8 & 3), rl, lo);
+      lds_f8(qt + (2 + (l8 >> 2)) * kBox, 2 * (l8 & 3), rl, hi);
+      if (p.has_norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(hi[e], hi[e], fmaf(lo[e], lo[e], ss));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float rn = rsqrtf(ss * (1.0f / kHD) + p.eps);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          lo[e] *= rn * wlo[e];
+          hi[e] *= rn * whi[e];
+        }
+      }
+      if (p.has_rotary) {
+        float c[8], sn[8];
+        const long long cb = (long long)(past + r / p.G) * (kHD / 2) + 8 * l8;
+        ld_f8(cbase + cb, c);
+        ld_f8(sbase + cb, sn);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float a = lo[e], b = hi[e];
+          lo[e] = fmaf(a, c[e], -b * sn[e]);
+          hi[e] = fmaf(b, c[e], a * sn[e]);
+        }
+      }
+      float mx = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        lo[e] *= klo[e];
+        hi[e] *= khi[e];
+        mx = fmax3(mx, fabsf(lo[e]), fabsf(hi[e]));
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      // 2^e <= mx < 2^(e+1) from the exponent bits (mx = 0 or subnormal: e = 0).
+      const int ebits = (__float_as_int(mx) >> 23) & 0xff;
+      const int e = ebits == 0 ? 0 : ebits - 127;
+      const float down = __int_as_float((127 - e) << 23);
+      uint32_t hw[2][4], lw[2][4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float* x = half == 0 ? lo : hi;
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const float a = x[2 * k2] * down, b = x[2 * k2 + 1] * down;
+          const __half2 hh = __floats2half2_rn(a, b);
+          const float2 hf = __half22float2(hh);
+          const __half2 ll = __floats2half2_rn(a - hf.x, b - hf.y);
+          hw[half][k2] = *reinterpret_cast<const uint32_t*>(&hh);
+          lw[half][k2] = *reinterpret_cast<const uint32_t*>(&ll);
+        }
+      }
+      __syncwarp();   // every lane of the row has read its values
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        *reinterpret_cast<uint4*>(qt + half * kBox + sw128_offset(rl, l8)) =
+            make_uint4(hw[half][0], hw[half][1], hw[half][2], hw[half][3]);
+        *reinterpret_cast<uint4*>(qt + (2 + half) * kBox + sw128_offset(rl, l8)) =
+            make_uint4(lw[half][0], lw[half][1], lw[half][2], lw[half][3]);
+      }
+      if (l8 == 0) sm.rho[tile][rl] = __int_as_float((127 + e) << 23);
     }
-    const int bx = c16 >> 3, ch = c16 & 7;
-    *reinterpret_cast<uint4*>(qt + bx * kBox + sw128_offset(rl, ch)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(qt + (2 + bx) * kBox + sw128_offset(rl, ch)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    fence_async_smem();   // rewritten tile (generic stores) -> async proxy: the S MMAs may read it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.q_ready[tile]);
   }
-  return up;
 }
 
 // BITS: 8 (int8 cache) or 4 (4-bit cache). PLAIN: no softcap and no bias
@@ -268,9 +314,7 @@ __device__ float split_query_row(const Params& p, uint8_t* qt, int rl, int g, in
 // bias are applied per thread in the max pass and written back to tensor memory.
 template <int BITS, bool PLAIN>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv) {
-  constexpr uint32_t kCodeBytes = 128u * (BITS == 8 ? 128u : 64u);   // one code tile
+prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmo) {
   extern __shared__ uint8_t smem_raw[];
   QcSmem& sm = *reinterpret_cast<QcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -309,18 +353,14 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
   if (tid == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.q_land[t], 1);
-      mbar_init(&sm.q_ready[t], 4);   // one arrival per softmax warp of the tile
+      mbar_init(&sm.q_ready[t], 8);   // one arrival per softmax warp
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_full[t], kBM);
       mbar_init(&sm.o_done[t], 1);
+      mbar_init(&sm.kf_full[t], kConvWarps);   // one arrival per converter warp
+      mbar_init(&sm.kf_empty[t], 1);  // MMA commits
     }
-    mbar_init(&sm.kc_full, 1);
-    mbar_init(&sm.vc_full, 1);
-    mbar_init(&sm.kc_empty, 2);       // one arrival per converter warp
-    mbar_init(&sm.vc_empty, 2);
-    mbar_init(&sm.kf_full, 2);
-    mbar_init(&sm.vf_full, 2);
-    mbar_init(&sm.kf_empty, 1);       // MMA commits
+    mbar_init(&sm.vf_full, kConvWarps);
     mbar_init(&sm.vf_empty, 1);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
@@ -330,10 +370,10 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const int krow0 = bg * p.C + kmin;   // cache row of the first key
+  const long long krow0 = (long long)bg * p.C + kmin;   // cache row of the first key
 
   if (warp == 0) {
-    // ================================================================ TMA producer
+    // ================================================================ TMA: query tiles
     if (elect_one()) {
       for (int q = 0; q < 2; ++q) {
         mbar_arrive_tx(&sm.q_land[q], kQRegion);
@@ -342,46 +382,20 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
       }
     }
     __syncwarp();
-    int issued_k = 0, issued_v = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      if (t == p.withhold_tile) break;   // testing: no copy of this tile, its waits expire
-      const uint32_t pe = ((uint32_t)t & 1u) ^ 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.kc_empty, pe, p.wait_budget)) || aborted(sm)) {
-        if (lane == 0) set_abort(p, sm);
-        break;
-      }
-      if (elect_one()) {
-        mbar_arrive_tx(&sm.kc_full, kCodeBytes);
-        tma_load_2d(sm.kc, &tmk, 0, krow0 + t * kBN, &sm.kc_full);
-      }
-      __syncwarp();
-      issued_k = t + 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sm.vc_empty, pe, p.wait_budget)) || aborted(sm)) {
-        if (lane == 0) set_abort(p, sm);
-        break;
-      }
-      if (elect_one()) {
-        mbar_arrive_tx(&sm.vc_full, kCodeBytes);
-        tma_load_2d(sm.vc, &tmv, 0, krow0 + t * kBN, &sm.vc_full);
-      }
-      __syncwarp();
-      issued_v = t + 1;
-    }
-    // Drain: no copy of this CTA may still be landing when it exits (the last
-    // copy of each staging buffer completes the phase of its index).
+    // No copy of this CTA may still be landing when it exits.
     mbar_wait(&sm.q_land[0], 0, p.wait_budget);
     mbar_wait(&sm.q_land[1], 0, p.wait_budget);
-    if (issued_k > 0) mbar_wait(&sm.kc_full, (uint32_t)(issued_k - 1) & 1u, p.wait_budget);
-    if (issued_v > 0) mbar_wait(&sm.vc_full, (uint32_t)(issued_v - 1) & 1u, p.wait_budget);
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    const uint64_t dk = desc_kmajor_sw128(smem_addr(sm.kf));
-    const uint64_t dv = desc_mnmajor_sw128(smem_addr(sm.vf), kBox, 1024);
-    uint64_t dq[2];
+    uint64_t dk[2], dq[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) dq[i] = desc_kmajor_sw128(smem_addr(sm.q[i]));
+    for (int i = 0; i < 2; ++i) {
+      dk[i] = desc_kmajor_sw128(smem_addr(sm.kf[i]));
+      dq[i] = desc_kmajor_sw128(smem_addr(sm.q[i]));
+    }
+    const uint64_t dv = desc_mnmajor_sw128(smem_addr(sm.vf), kBox, 1024);
     // S_q = Q_hi K^T + Q_lo K^T (the lo tile starts 32 KB after the hi tile).
-    auto issue_s = [&](int q) {
+    auto issue_s = [&](int q, int kb) {
       const uint32_t d = tmem + q * 128;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
@@ -389,7 +403,7 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t off = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
-          mma_f16_ss(d, a0 + off, dk + off, kIdS, part > 0 || ks > 0);
+          mma_f16_ss(d, a0 + off, dk[kb] + off, kIdS, part > 0 || ks > 0);
         }
       }
       mma_commit(&sm.s_full[q]);
@@ -409,22 +423,24 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
       mma_commit(&sm.o_done[q]);
     };
     bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_ready[0], 0, p.wait_budget) &&
-                                          mbar_wait(&sm.kf_full, 0, p.wait_budget));
+                                          mbar_wait(&sm.kf_full[0], 0, p.wait_budget));
     if (ok && elect_one()) {
       tc_fence_after();
-      issue_s(0);
+      issue_s(0, 0);
     }
     __syncwarp();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_ready[1], 0, p.wait_budget));
     if (ok && elect_one()) {
       tc_fence_after();
-      issue_s(1);
-      mma_commit(&sm.kf_empty);
+      issue_s(1, 0);
+      mma_commit(&sm.kf_empty[0]);
     }
     __syncwarp();
     for (int t = 0; t < ntiles && ok; ++t) {
       const uint32_t tp = (uint32_t)t & 1u;
       const bool more = t + 1 < ntiles;
+      const int kb1 = (t + 1) & 1;                                 // K buffer of tile t+1
+      const uint32_t kp1 = (uint32_t)((t + 1) >> 1) & 1u;          // its use parity
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.vf_full, tp, p.wait_budget) &&
                                        mbar_wait(&sm.p_full[0], tp, p.wait_budget))) {
         ok = false;
@@ -435,13 +451,13 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
         issue_pv(0, t > 0);
       }
       __syncwarp();
-      if (more && !__all_sync(0xffffffffu, mbar_wait(&sm.kf_full, tp ^ 1u, p.wait_budget))) {
+      if (more && !__all_sync(0xffffffffu, mbar_wait(&sm.kf_full[kb1], kp1, p.wait_budget))) {
         ok = false;
         break;
       }
       if (more && elect_one()) {
         tc_fence_after();
-        issue_s(0);
+        issue_s(0, kb1);
       }
       __syncwarp();
       if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[1], tp, p.wait_budget))) {
@@ -453,8 +469,8 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
         issue_pv(1, t > 0);
         mma_commit(&sm.vf_empty);
         if (more) {
-          issue_s(1);
-          mma_commit(&sm.kf_empty);
+          issue_s(1, kb1);
+          mma_commit(&sm.kf_empty[kb1]);
         }
       }
       __syncwarp();
@@ -469,32 +485,58 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
     __syncwarp();
   } else if (warp >= kConvWarp0) {
     // ================================================================ converters
-    // Order: K(0), then per tile t: V(t) (its buffer is free once P_1.V(t-1)
-    // is done) and K(t+1) (free once S_1(t) is done).
-    const int row0 = (warp - kConvWarp0) * 64;
-    auto convert = [&](bool is_k, int u) -> bool {
-      const uint32_t pf = (uint32_t)u & 1u;
-      uint64_t* cfull = is_k ? &sm.kc_full : &sm.vc_full;
-      uint64_t* fempty = is_k ? &sm.kf_empty : &sm.vf_empty;
-      if (!__all_sync(0xffffffffu, mbar_wait(cfull, pf, p.wait_budget) && mbar_wait(fempty, pf ^ 1u, p.wait_budget)) ||
-          aborted(sm))
+    // Conversion order: K(0), then K(t+1) (its buffer is free once S_1(t-1)
+    // is done), V(t) (free once P_1.V(t-1) is done). The codes of the next
+    // conversion are loaded while the current one waits and converts.
+    constexpr int kSteps = kConvRows * (BITS == 8 ? 8 : 4) / 32;
+    const int row0 = (warp - kConvWarp0) * kConvRows;
+    const long long ncache = (long long)p.B * p.Nkv * p.C;
+    const uint8_t* kcache = static_cast<const uint8_t*>(p.present_k);
+    const uint8_t* vcache = static_cast<const uint8_t*>(p.present_v);
+    const int nconv = 2 * ntiles;
+    // item n: 0 -> K(0); 2t+1 -> K(t+1) (V(t) when t is the last tile); 2t+2 -> V(t)
+    auto item = [&](int n, bool& is_k) -> int {
+      if (n == 0) {
+        is_k = true;
+        return 0;
+      }
+      const int t = (n - 1) >> 1;
+      is_k = ((n - 1) & 1) == 0 && t + 1 < ntiles;
+      return is_k ? t + 1 : t;
+    };
+    auto load = [&](int n, uint4* w) {
+      bool is_k;
+      const int u = item(n, is_k);
+      load_codes<BITS>(is_k ? kcache : vcache, krow0 + (long long)u * kBN, ncache, row0, lane, w);
+    };
+    bool withheld = false;
+    auto convert = [&](int n, const uint4* w) -> bool {
+      bool is_k;
+      const int u = item(n, is_k);
+      if (u == p.withhold_tile) {   // testing: this tile is never converted, the waits for it expire
+        withheld = true;
         return false;
-      tc_fence_after();
-      convert_rows<BITS>(is_k ? sm.kc : sm.vc, is_k ? sm.kf : sm.vf, row0, lane);
+      }
+      uint64_t* empty = is_k ? &sm.kf_empty[u & 1] : &sm.vf_empty;
+      const uint32_t pe = (is_k ? (uint32_t)(u >> 1) : (uint32_t)u) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(empty, pe ^ 1u, p.wait_budget)) || aborted(sm)) return false;
+      store_codes_h<BITS>(w, is_k ? sm.kf[u & 1] : sm.vf, row0, lane);
       fence_async_smem();   // fp16 tile (generic stores) -> async proxy: the MMAs may read it
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(is_k ? &sm.kf_full : &sm.vf_full);
-        mbar_arrive(is_k ? &sm.kc_empty : &sm.vc_empty);
-      }
+      if (lane == 0) mbar_arrive(is_k ? &sm.kf_full[u & 1] : &sm.vf_full);
       return true;
     };
-    bool ok = convert(true, 0);
-    for (int t = 0; t < ntiles && ok; ++t) {
-      ok = convert(false, t);
-      if (ok && t + 1 < ntiles) ok = convert(true, t + 1);
+    uint4 wa[kSteps], wb[kSteps];
+    bool ok = true;
+    load(0, wa);
+    for (int n = 0; n < nconv && ok; n += 2) {
+      if (n + 1 < nconv) load(n + 1, wb);
+      ok = convert(n, wa);
+      if (!ok || n + 1 >= nconv) break;
+      if (n + 2 < nconv) load(n + 2, wa);
+      ok = convert(n + 1, wb);
     }
-    if (!ok && lane == 0) set_abort(p, sm);
+    if (!ok && !withheld && lane == 0) set_abort(p, sm);
   } else {
     // ================================================================ softmax groups
     const int q = (warp - 2) >> 2;            // query tile of this group
@@ -512,20 +554,15 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
     const uint32_t s_addr = tmem + lane_addr + q * 128;
     const uint32_t o_addr = tmem + lane_addr + 256 + q * 128;
     const bool cap = p.softcap > 0.f;
-    const float qscale = cap ? p.scale : p.scale * kLog2e;
     const float* bias_row = nullptr;
     if (!PLAIN && p.has_bias && live)
       bias_row = reinterpret_cast<const float*>(p.bias) +
                  (((long long)(p.bias_bdim > 1 ? b : 0) * p.bias_ndim + (p.bias_ndim > 1 ? h : 0)) * p.S + i) *
                      p.bias_ld;
 
-    // ---- this thread's query row -> hi / lo operand rows, in place
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_land[q], 0, p.wait_budget));
-    if (!ok && lane == 0) set_abort(p, sm);
-    const float rho = split_query_row(p, sm.q[q], rl, g, pos, qscale);
-    fence_async_smem();   // rewritten rows (generic stores) -> async proxy: the S MMAs may read them
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.q_ready[q]);
+    split_query_tiles(p, sm, past, r0, nrows, g, tid - 64, cap ? p.scale : p.scale * kLog2e);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_ready[q], 0, p.wait_budget));   // rho of every row written
+    const float rho = sm.rho[q][rl];
 
     // Score of column e in the log2 domain: S rho (plain); with softcap c the
     // tanh form on S rho = scale q.k, then + bias log2(e).
@@ -541,34 +578,42 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
       const int j0 = kmin + t * kBN;
       const int lo = max(lo_key - j0, 0), hi = min(hi_key - j0, kBN);   // visible columns [lo, hi)
       const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kBN);
-      // Pass 1: row max. Masked columns (and, with softcap / bias, every
-      // transformed score) are written back so that pass 2 is the same for all.
+      // Pass 1: row max, 64 columns at a time. Masked columns (and, with
+      // softcap / bias, every transformed score) are written back so that
+      // pass 2 is the same for all.
       float mt;
       {
-        uint32_t x[kBN];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, x + c * 32);
-        tmem_ld_wait();
-        if constexpr (!PLAIN) {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e) {
-            float v = __uint_as_float(x[e]) * k_raw;
-            if (cap) v = fmaf(__frcp_rn(ex2(v) + 1.0f), k_mul, k_add);
-            if (bias_row != nullptr && e >= lo && e < hi) v = fmaf(bias_row[j0 + e], kLog2e, v);
-            x[e] = __float_as_uint(v);
-          }
-        }
-        if (!PLAIN || !full) {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e) x[e] = (e >= lo && e < hi) ? x[e] : 0xff800000u;   // -inf
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_st32(s_addr + c * 32, x + c * 32);
-          tmem_st_wait();
-        }
         float m4[4] = {kNegBig, kNegBig, kNegBig, kNegBig};   // four independent chains
 #pragma unroll
-        for (int e = 0; e < kBN; e += 2)
-          m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t x[64];
+          tmem_ld32(s_addr + hf * 64, x);
+          tmem_ld32(s_addr + hf * 64 + 32, x + 32);
+          tmem_ld_wait();
+          if constexpr (!PLAIN) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const int col = hf * 64 + e;
+              float v = __uint_as_float(x[e]) * k_raw;
+              if (cap) v = fmaf(__frcp_rn(ex2(v) + 1.0f), k_mul, k_add);
+              if (bias_row != nullptr && col >= lo && col < hi) v = fmaf(bias_row[j0 + col], kLog2e, v);
+              x[e] = __float_as_uint(v);
+            }
+          }
+          if (!PLAIN || !full) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const int col = hf * 64 + e;
+              x[e] = (col >= lo && col < hi) ? x[e] : 0xff800000u;   // -inf
+            }
+            tmem_st32(s_addr + hf * 64, x);
+            tmem_st32(s_addr + hf * 64 + 32, x + 32);
+          }
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], __uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+        }
+        if (!PLAIN || !full) tmem_st_wait();
         const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         mt = m > kNegBig ? (PLAIN ? m * k_raw : m) : kNegBig;   // k_raw = rho > 0 in the plain form
       }
@@ -602,31 +647,36 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
         tmem_ld32(s_addr + hf * 64, x);
         tmem_ld32(s_addr + hf * 64 + 32, x + 32);
         tmem_ld_wait();
-        uint32_t ph[32], pl[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float2 arg = ffma2(make_float2(__uint_as_float(x[2 * k]), __uint_as_float(x[2 * k + 1])), mul22, negm2);
-          const float pa = ex2(arg.x), pb = ex2(arg.y);
-          ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
-          const __half2 hp = __floats2half2_rn(pa, pb);
-          const float2 hf2 = __half22float2(hp);
-          const __half2 lp = __floats2half2_rn(pa - hf2.x, pb - hf2.y);
-          ph[k] = *reinterpret_cast<const uint32_t*>(&hp);
-          pl[k] = *reinterpret_cast<const uint32_t*>(&lp);
+        for (int qq = 0; qq < 2; ++qq) {   // keys 32 qq .. 32 qq + 31 of the half
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int e = 32 * qq + 2 * k;
+            const float2 arg = ffma2(make_float2(__uint_as_float(x[e]), __uint_as_float(x[e + 1])), mul22, negm2);
+            const float pa = ex2(arg.x), pb = ex2(arg.y);
+            ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
+            const __half2 hp = __floats2half2_rn(pa, pb);
+            const float2 hf2 = __half22float2(hp);
+            const __half2 lp = __floats2half2_rn(pa - hf2.x, pb - hf2.y);
+            ph[k] = *reinterpret_cast<const uint32_t*>(&hp);
+            pl[k] = *reinterpret_cast<const uint32_t*>(&lp);
+          }
+          tmem_st16(s_addr + hf * 64 + 16 * qq, ph);
+          tmem_st16(s_addr + hf * 64 + 32 + 16 * qq, pl);
         }
-        tmem_st32(s_addr + hf * 64, ph);
-        tmem_st32(s_addr + hf * 64 + 32, pl);
       }
       l_run += ls2.x + ls2.y;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm.p_full[q]);
     }
-    // ---- epilogue: O / l (+ sink) times the V channel scales, fp32, one row per thread
+    // ---- epilogue: O / l (+ sink) times the V channel scales, fp32. Each
+    // thread stages its row in the group's query region (free: every S MMA of
+    // the group is done once its last P.V is) in the copied layout, and one
+    // thread writes the tile with four tensor stores (rows past S are skipped).
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(ntiles - 1) & 1u, p.wait_budget) && !aborted(sm));
-    if (!ok) {
-      set_abort(p, sm);
-    } else {
+    if (ok) {
       tc_fence_after();
       float mf = m_run, extra = 0.f;
       if (p.has_sink || p.smooth) {
@@ -637,26 +687,35 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
       const float f = ex2(m_run - mf);
       const float den = l_run * f + extra;
       const float scale_out = (live && den > 0.f) ? f / den : 0.f;
-      float* orow = reinterpret_cast<float*>(p.out) + ((long long)(b * p.S + i) * p.N + h) * kHD;
-      const float* vs = p.v_scale + (p.v_scale_n == 1 ? 0 : g * kHD);
-      const int vstep = p.v_scale_n == 1 ? 0 : 1;
+      const bool vch = p.v_scale_n != 1;
+      const float so = vch ? scale_out : scale_out * p.v_scale[0];
+      const float4* vs4 = reinterpret_cast<const float4*>(p.v_scale + (vch ? g * kHD : 0));
+      uint8_t* stage = sm.q[q];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; ++c) {          // box c: dims 32 c .. 32 c + 31
         uint32_t raw[32];
-        tmem_ld32(o_addr + c * 32, raw);   // all lanes (warp-wide); only real rows store
+        tmem_ld32(o_addr + c * 32, raw);
         tmem_ld_wait();
-        if (!row_ok) continue;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const int d = c * 32 + e;
+          const float4 v = vch ? __ldg(vs4 + (c * 32 + e) / 4) : make_float4(1.f, 1.f, 1.f, 1.f);
           float4 o;
-          o.x = __uint_as_float(raw[e]) * scale_out * __ldg(vs + vstep * d);
-          o.y = __uint_as_float(raw[e + 1]) * scale_out * __ldg(vs + vstep * (d + 1));
-          o.z = __uint_as_float(raw[e + 2]) * scale_out * __ldg(vs + vstep * (d + 2));
-          o.w = __uint_as_float(raw[e + 3]) * scale_out * __ldg(vs + vstep * (d + 3));
-          *reinterpret_cast<float4*>(orow + d) = o;
+          o.x = __uint_as_float(raw[e]) * so * v.x;
+          o.y = __uint_as_float(raw[e + 1]) * so * v.y;
+          o.z = __uint_as_float(raw[e + 2]) * so * v.z;
+          o.w = __uint_as_float(raw[e + 3]) * so * v.w;
+          *reinterpret_cast<float4*>(stage + c * kBox + sw128_offset(rl, e >> 2)) = o;
         }
       }
+      fence_async_smem();   // staged rows (generic stores) -> async proxy: the tensor stores read them
+    }
+    const bool all_ok = group_all(ok, q);
+    if (!all_ok) {
+      if (lane == 0) set_abort(p, sm);
+    } else if (quarter == 2 && elect_one()) {   // warp 2 (group 0) or 6 (group 1)
+      for (int k = 0; k < 4; ++k) tma_store_4d(&tmo, sm.q[q] + k * kBox, 32 * k, g * p.G, (r0 + q * kBM) / p.G, b);
+      bulk_commit();
+      bulk_wait_read();   // the staged tile is read before the CTA may exit
     }
   }
   tc_fence_before();
@@ -672,13 +731,10 @@ bool prefill_tcq_supported(const Params& p) {
 }
 
 cudaError_t prepare_prefill_tcq(const Params& p, TmaMaps* maps) {
-  const uint64_t rows = (uint64_t)p.B * p.Nkv * p.C;
-  const uint32_t row_bytes = p.cache_type == kI8 ? 128u : 64u;
   cudaError_t e;
   if ((e = encode_f32_query_sw128(&maps->m[0], p.q, p.B, p.S, p.N, (uint32_t)p.G)) != cudaSuccess) return e;
-  if ((e = encode_u8_2d(&maps->m[1], p.present_k, rows, row_bytes, row_bytes, row_bytes, kBN)) != cudaSuccess) return e;
-  if ((e = encode_u8_2d(&maps->m[2], p.present_v, rows, row_bytes, row_bytes, row_bytes, kBN)) != cudaSuccess) return e;
-  maps->m[3] = maps->m[2];
+  if ((e = encode_f32_query_sw128(&maps->m[1], p.out, p.B, p.S, p.N, (uint32_t)p.G)) != cudaSuccess) return e;
+  maps->m[2] = maps->m[3] = maps->m[1];
   return cudaSuccess;
 }
 
@@ -704,7 +760,7 @@ cudaError_t launch_prefill_tcq(const Params& p, cudaStream_t st, const TmaMaps& 
   }
   const int nrows = p.S * p.G;
   dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
-  kern<<<grid, kThreads, smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2]);
+  kern<<<grid, kThreads, smem, st>>>(p, maps.m[0], maps.m[1]);
   return cudaGetLastError();
 }
 

@@ -224,8 +224,10 @@ GQA_API gqa_status gqa_forward_noalloc(gqa_handle* handle, const gqa_inputs* in,
  *     are then undefined. The next call on the handle and workspace is
  *     unaffected (each call clears the workspace header).
  *   withhold_copy: -1 (default) off; k >= 0 makes the TMA warp of every
- *     tensor-core CTA stop before the copy of its k-th key tile, so the waits
- *     for that tile expire: a test of the timeout path that faults nothing.
+ *     tensor-core CTA stop before the copy of its k-th key tile (in the
+ *     prefill over an int8 / 4-bit cache: the converter warps before its
+ *     conversion), so the waits for that tile expire: a test of the timeout
+ *     path that faults nothing.
  * Applies to the following gqa_forward / gqa_forward_noalloc calls on the
  * handle. Host-only; INVALID_ARGUMENT for a NULL handle or a value out of range. */
 GQA_API gqa_status gqa_set_wait_limit(gqa_handle* handle, int64_t cycles, int32_t withhold_copy);

@@ -1,13 +1,14 @@
 """Bounded waits of the tensor-core kernels, made to expire without any fault.
 
 With gqa_set_wait_limit(handle, 2e6 cycles, withhold_copy=0) the TMA warp of
-every tensor-core CTA stops before the copy of its first key tile, so the
-waits for that tile run out (about 1 ms each at the maximum clock). The call
+every tensor-core CTA stops before the copy of its first key tile (the
+converter warps before its conversion, in the prefill over an int8 cache), so
+the waits for that tile run out (about 1 ms each at the maximum clock). The call
 must return, the status word must report GQA_DEVICE_TIMEOUT, and an ordinary
 call right after, on the same handle and workspace, must match the oracle:
 tensor memory was freed and the merge tickets left behind are cleared by the
-next call. Covers the fp16 and the int8-cache decode kernels and the prefill
-kernel with and without the staged bias.
+next call. Covers the fp16 and the int8-cache decode kernels, the fp16 prefill
+kernel with and without the staged bias and the prefill over an int8 cache.
 """
 
 import time
@@ -29,6 +30,8 @@ CASES = {
                               seqlens_range=(200, 590), quant="PER_CHANNEL"), "decode_tensor_core"),
     "prefill_tc": (CaseSpec(name="to_pf", dtype="f16", B=1, S=200, N=8, Nkv=2, H=128, capacity=256, mode="prompt",
                             seqlens_k=(199,), rotary_theta=1e4, qk_norm=True), "prefill_tensor_core"),
+    "prefill_tc_int8_fp32": (CaseSpec(name="to_pq", dtype="f32", B=1, S=200, N=8, Nkv=2, H=128, capacity=256,
+                                      mode="prompt", seqlens_k=(199,), quant="PER_CHANNEL"), "prefill_tensor_core"),
     "prefill_tc_staged_bias": (CaseSpec(name="to_ch", dtype="f16", B=1, S=64, N=16, Nkv=2, H=128, capacity=600,
                                         mode="shared", seqlens_range=(300, 590), softcap=30.0, bias=(1, 1, 0.5),
                                         rotary_theta=1e4), "prefill_tensor_core"),
