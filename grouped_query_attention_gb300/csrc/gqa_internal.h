@@ -136,7 +136,7 @@ cudaError_t launch_bias_stage(const Params& p, cudaStream_t st);
 bool prefill_tc_bias_staged(const Params& p);
 
 struct TmaMaps {
-  CUtensorMap m[4];
+  CUtensorMap m[5];
 };
 cudaError_t prepare_decode_tc(const Params& p, TmaMaps* maps);
 cudaError_t launch_decode_tc(const Params& p, cudaStream_t st, const TmaMaps& maps);

@@ -187,6 +187,16 @@ __device__ __forceinline__ void set_abort(const Params& p, TcSmem& sm) {
   flag_status(p, GQA_DEVICE_TIMEOUT_BIT);
 }
 
+// All bits of `v` over the 128 threads of softmax group q (named barrier 1 + q).
+__device__ __forceinline__ bool group_all(bool v, int q) {
+  uint32_t r;
+  asm volatile("{ .reg .pred p, c; setp.ne.u32 c, %1, 0; bar.red.and.pred p, %2, 128, c; selp.u32 %0, 1, 0, p; }"
+               : "=r"(r)
+               : "r"((uint32_t)v), "r"(1 + q)
+               : "memory");
+  return r != 0;
+}
+
 // Eight fp16 values (16 bytes) as fp32, and back (round to nearest).
 __device__ __forceinline__ void ld_h8f(const __half* src, float* f) {
   const uint4 u = *reinterpret_cast<const uint4*>(src);
@@ -305,7 +315,8 @@ __device__ void transform_q_tiles(const Params& p, TcSmem& sm, int past, int r0,
 template <int MODE, bool CAP>
 __global__ void __launch_bounds__(threads_for(MODE), 1)
 prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmb) {
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmb,
+                  const __grid_constant__ CUtensorMap tmo) {
   constexpr bool PLAIN = MODE == kPlain;
   constexpr bool STAGED = MODE == kStagedBias;
   constexpr int kThreads = threads_for(MODE);
@@ -906,11 +917,14 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       tc_fence_before();
       mbar_arrive(&sm.p_full[q]);
     }
-    // ---- epilogue: O / l (+ sink), fp16, one row per thread
+    // ---- epilogue: O / l (+ sink), fp16, one row per thread. With raw query
+    // tiles (the group size divides 128) the rows are staged in the group's
+    // query tile (free: every S MMA of the group is done once its last P.V is),
+    // in the copied layout, and one thread writes the tile with two tensor
+    // stores (rows past S are skipped); otherwise each thread stores its row.
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(ntiles - 1) & 1u, p.wait_budget) && !aborted(sm));
-    if (!ok) {
-      set_abort(p, sm);
-    } else {
+    float scale_out = 0.f;
+    if (ok) {
       tc_fence_after();
       float mf = m_run, extra = 0.f;
       if (p.has_sink || p.smooth) {
@@ -920,7 +934,39 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
       }
       const float f = ex2(m_run - mf);
       const float den = l_run * f + extra;
-      const float scale_out = (live && den > 0.f) ? f / den : 0.f;
+      scale_out = (live && den > 0.f) ? f / den : 0.f;
+    }
+    if (p.q_in_prefill) {
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(o_addr + c * 32, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {   // dims 32 c + e .. : box (32 c + e) / 64, chunk ((32 c + e) % 64) / 8
+            uint4 u;
+            __half2* h2 = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              h2[k] = __floats2half2_rn(__uint_as_float(raw[e + 2 * k]) * scale_out,
+                                        __uint_as_float(raw[e + 2 * k + 1]) * scale_out);
+            const int d = c * 32 + e;
+            *reinterpret_cast<uint4*>(sm.q[q] + (d >> 6) * kBox + sw128_offset(rl, (d & 63) >> 3)) = u;
+          }
+        }
+        fence_async_smem();   // staged rows (generic stores) -> async proxy: the tensor stores read them
+      }
+      if (!group_all(ok, q)) {
+        if (lane == 0) set_abort(p, sm);
+      } else if (quarter == 2 && elect_one()) {   // warp 2 (group 0) or 6 (group 1)
+        for (int bx = 0; bx < 2; ++bx) tma_store_4d(&tmo, sm.q[q] + bx * kBox, 64 * bx, g * p.G, (r0 + q * kBM) / p.G, b);
+        bulk_commit();
+        bulk_wait_read();   // the staged tile is read before the CTA may exit
+      }
+    } else if (!ok) {
+      set_abort(p, sm);
+    } else {
       __half* orow = reinterpret_cast<__half*>(p.out) + ((long long)(b * p.S + i) * p.N + h) * kHD;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -968,8 +1014,10 @@ cudaError_t prepare_prefill_tc(const Params& p, TmaMaps* maps) {
     return e;
   if ((e = encode_fp16_2d_sw128(&maps->m[2], vsrc, (uint64_t)krows, kHD, kHD * 2, 64, kBN)) != cudaSuccess)
     return e;
+  maps->m[4] = maps->m[2];   // a valid map in the output slot when the epilogue stores per thread (never read)
   if (p.q_in_prefill) {
     if ((e = encode_fp16_query_sw128(&maps->m[0], p.q, p.B, p.S, p.N, (uint32_t)p.G)) != cudaSuccess) return e;
+    if ((e = encode_fp16_query_sw128(&maps->m[4], p.out, p.B, p.S, p.N, (uint32_t)p.G)) != cudaSuccess) return e;
   } else {
     const long long qrows = (long long)p.B * p.Nkv * p.S * p.G;
     if ((e = encode_fp16_2d_sw128(&maps->m[0], p.qprep, (uint64_t)qrows, kHD, kHD * 2, 64, kBM)) != cudaSuccess)
@@ -1008,7 +1056,7 @@ cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& m
   }
   const int nrows = p.S * p.G;
   dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
-  kern<<<grid, threads_for(mode), smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2], maps.m[3]);
+  kern<<<grid, threads_for(mode), smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.m[4]);
   return cudaGetLastError();
 }
 
