@@ -382,7 +382,7 @@ def measure_workload(name: str, args, world: int, rank: int, local: int) -> dict
     peaks, peaks_src = load_peaks()
     # The sources a kernel's code comes from (a traffic record holds only while they are unchanged).
     shared = ["common.cuh", "gqa_internal.h"]
-    tc_decode_src = ["decode_tc_i8.cu" if sp.quant != "NONE" else "decode_tc.cu", "tcgen05.cuh"]
+    tc_decode_src = ["decode_tc.cu", "tcgen05.cuh"]
     tc_prefill_src = "prefill_tcq.cu" if sp.quant != "NONE" and sp.dtype == "f32" else "prefill_tc.cu"
     kernel_src = {"decode": ["decode.cu"], "decode_tensor_core": tc_decode_src,
                   "prefill_tensor_core": [tc_prefill_src, "tcgen05.cuh"],

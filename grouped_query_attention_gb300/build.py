@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgqa_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["gqa_api.cu", "prepass.cu", "decode.cu", "prefill_simt.cu", "prefill_tc.cu", "prefill_tcq.cu", "decode_tc.cu", "decode_tc_i8.cu", "tma_host.cu"]
+SOURCES = ["gqa_api.cu", "prepass.cu", "decode.cu", "prefill_simt.cu", "prefill_tc.cu", "prefill_tcq.cu", "decode_tc.cu", "tma_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
