@@ -256,3 +256,28 @@ def test_bad_seqlens_sets_device_status():
     assert gpu["status"] & 1
     # batch 1 is untouched
     assert np.array_equal(gpu["present_key"][1], case["inputs"]["past_key"][1])
+
+
+@pytest.mark.parametrize("name", ["f16_tc_all_features", "i8_per_tensor_prefill_all_features"])
+def test_bad_seqlens_prefill_skips_one_batch_entry(name):
+    """A prefill with one batch entry's seqlens_k beyond the cache: that entry is skipped and flagged,
+    the others match the oracle (outputs of every row, caches byte for byte), and the skipped
+    entry's cache rows keep their bytes (tensor-core prefill, fp16 and over an int8 cache)."""
+    case = generate(PREFILL[name], seed=25)
+    good = case["inputs"]["seqlens_k"].copy()
+    case["inputs"]["seqlens_k"] = good.copy()
+    case["inputs"]["seqlens_k"][1] = 10_000   # beyond total_sequence_length and the capacity
+    gpu = run_gpu(case)
+    assert gpu["status"] & 1
+    case["inputs"]["seqlens_k"] = good
+    B, S = case["inputs"]["query"].shape[:2]
+    N = case["attrs"]["num_heads"]
+    ok = valid_rows(case)
+    sample = [(b, h, i) for b in (0, 2) for h in range(N) for i in range(S) if ok[b, i]]
+    ref = run_oracle(case, sample=sample)
+    check_output(case, gpu, ref, sample=sample)
+    for nm in ("present_key", "present_value"):
+        for b in (0, 2):
+            assert np.array_equal(gpu[nm][b].view(np.uint8), ref[nm][b].view(np.uint8)), f"{nm}[{b}]"
+        untouched = case["inputs"]["past_key" if nm == "present_key" else "past_value"][1]
+        assert np.array_equal(gpu[nm][1].view(np.uint8), untouched.view(np.uint8)), f"{nm}[1] changed"
