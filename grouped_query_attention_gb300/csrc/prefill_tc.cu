@@ -95,15 +95,14 @@ __device__ __forceinline__ float rcp_approx(float x) {
 //   softcap c:  c * tanh(raw * scale / c) * log2(e) + bias * log2(e), with
 //               tanh(u) = 1 - 2 / (exp(2u) + 1): e2 = exp2(raw * k_exp),
 //               x = c log2(e) - 2 c log2(e) / (e2 + 1).
-//   softcap, |u| = |raw * scale / c| <= 1/4 (every lane of a warp): the
+//   softcap, |u| = |raw * scale / c| <= 1/8 (every lane of a warp): the
 //               same value on the FMA pipe, c tanh(u) log2(e) =
 //               raw * scale * log2(e) * P(u^2), P below.
-// tanh(u) / u = P(u^2) for |u| <= 1/4: degree-3 least-squares fit in z = u^2
-// over [0, 1/16] (Chebyshev nodes, weighted for relative error), coefficients
-// rounded to fp32: relative error 3.6e-9 in exact arithmetic.
-constexpr float kTanhP1 = -3.333323896e-01f;
-constexpr float kTanhP2 = 1.332412809e-01f;
-constexpr float kTanhP3 = -5.141825974e-02f;
+// tanh(u) / u = P(u^2) for |u| <= 1/8: degree-2 least-squares fit in z = u^2
+// over [0, 1/64] (Chebyshev nodes, weighted for relative error), coefficients
+// rounded to fp32: relative error 8.1e-9 in exact arithmetic.
+constexpr float kTanhP1 = -3.3332762e-01f;
+constexpr float kTanhP2 = 1.3216068e-01f;
 
 struct ScoreConst {
   float k_raw;    // raw multiplier: scale * log2(e) (no softcap) or 2 * scale * log2(e) / c
@@ -113,8 +112,8 @@ struct ScoreConst {
   // c tanh(u) log2(e) = x Q(x^2), Q(y) = sum_n C_n y^n with
   // C_n = scale log2(e) P_n (scale / c)^(2n) (P_0 = 1), so neither u nor the
   // final scale costs an operation per score.
-  float c3[4];
-  float y3;       // validity: x^2 <= (1/16) (c / scale)^2, i.e. |u| <= 1/4
+  float cq[3];
+  float yq;       // validity: x^2 <= (1/64) (c / scale)^2, i.e. |u| <= 1/8
 };
 
 __device__ __forceinline__ ScoreConst score_const(const Params& p) {
@@ -124,25 +123,24 @@ __device__ __forceinline__ ScoreConst score_const(const Params& p) {
   k.k_add = p.softcap * kLog2e;
   const float ku = p.softcap > 0.f ? p.scale / p.softcap : 0.f;
   const float ku2 = ku * ku, kw = p.scale * kLog2e;
-  const float p3[4] = {1.f, kTanhP1, kTanhP2, kTanhP3};
+  const float pn[3] = {1.f, kTanhP1, kTanhP2};
   float pw = 1.f;
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    k.c3[n] = kw * p3[n] * pw;
+  for (int n = 0; n < 3; ++n) {
+    k.cq[n] = kw * pn[n] * pw;
     pw *= ku2;
   }
-  k.y3 = ku2 > 0.f ? 0.0625f / ku2 : INFINITY;
+  k.yq = ku2 > 0.f ? 0.015625f / ku2 : INFINITY;
   return k;
 }
 
 // Softcapped scores of two raw products on the FMA pipe, log2 domain, plus
 // `add` (the bias in the log2 domain) in the last fused multiply-add; the
-// squared raw products are returned for the validity check (x^2 <= y3).
+// squared raw products are returned for the validity check (x^2 <= yq).
 __device__ __forceinline__ float2 softcap_poly2(float2 raw, const ScoreConst& k, float2& y, float2 add) {
   y = ffma2(raw, raw, make_float2(0.f, 0.f));
-  float2 q = ffma2(y, make_float2(k.c3[3], k.c3[3]), make_float2(k.c3[2], k.c3[2]));
-  q = ffma2(q, y, make_float2(k.c3[1], k.c3[1]));
-  q = ffma2(q, y, make_float2(k.c3[0], k.c3[0]));
+  float2 q = ffma2(y, make_float2(k.cq[2], k.cq[2]), make_float2(k.cq[1], k.cq[1]));
+  q = ffma2(q, y, make_float2(k.cq[0], k.cq[0]));
   return ffma2(raw, q, add);
 }
 
@@ -748,7 +746,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           tmem_ld32(s_h + 32, r + 32);
           tmem_ld_wait();
           // Transform the half in place: scale, softcap, bias. With a softcap the
-          // FMA-pipe polynomial goes first and is checked afterwards (|u| <= 1/4
+          // FMA-pipe polynomial goes first and is checked afterwards (|u| <= 1/8
           // on every lane of the warp, from the largest raw^2); otherwise the raw
           // scores are read again from tensor memory (intact: P of this half is
           // written after it) and take the exp2 / reciprocal form.
@@ -819,7 +817,7 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
           };
           if constexpr (CAP) {
             const float zmax = transform(true);
-            if (__any_sync(0xffffffffu, !(zmax <= kc.y3))) {
+            if (__any_sync(0xffffffffu, !(zmax <= kc.yq))) {
               tmem_ld32(s_h, r);
               tmem_ld32(s_h + 32, r + 32);
               tmem_ld_wait();
