@@ -360,10 +360,26 @@ def measure_workload(name: str, args, world: int, rank: int, local: int) -> dict
     ms = max_over_ranks(ms_local, world, device)
     assert op.device_status() == 0, f"{name}: device status set during the timed steps"
 
-    # ---- end to end through the public API with host buffers (pinned), copies in the timed region
-    host_in = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory() for k in ("query", "key", "value", "seqlens_k")}
+    # ---- end to end through the public API with host buffers (pinned), copies in the timed region.
+    # The step's inputs (query, key, value, seqlens_k) sit back to back in one pinned host buffer
+    # and land with one copy in one device buffer whose views the call takes, as a serving loop
+    # batches its small transfers; the output comes back with one copy.
+    names = ("query", "key", "value", "seqlens_k")
+    arrs = [np.ascontiguousarray(inp[k]) for k in names]
+    offs, stage_bytes = [], 0
+    for a in arrs:
+        offs.append(stage_bytes)
+        stage_bytes += (a.nbytes + 255) // 256 * 256
+    host_stage = torch.empty(stage_bytes, dtype=torch.uint8).pin_memory()
+    dev_stage = torch.empty(stage_bytes, dtype=torch.uint8, device=device)
+    staged = {}
+    for k, a, o in zip(names, arrs, offs):
+        host_stage[o:o + a.nbytes].copy_(torch.from_numpy(a.reshape(-1).view(np.uint8)))
+        staged[k] = dev_stage[o:o + a.nbytes].view(dev[k].dtype).view(dev[k].shape)
+    call_e2e = dict(call, query=staged["query"], key=staged["key"], value=staged["value"],
+                    seqlens_k=staged["seqlens_k"])
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = stage_bytes
     d2h = host_out.numel() * host_out.element_size()
     e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -372,9 +388,8 @@ def measure_workload(name: str, args, world: int, rank: int, local: int) -> dict
     for k in range(args.steps):
         flush_l2()
         e_starts[k].record(stream)
-        for key_name, t in host_in.items():
-            dev[key_name].copy_(t, non_blocking=True)
-        step()
+        dev_stage.copy_(host_stage, non_blocking=True)
+        op(workspace=ws, **call_e2e)
         host_out.copy_(out, non_blocking=True)
         e_ends[k].record(stream)
     torch.cuda.synchronize()
@@ -465,7 +480,7 @@ def measure_workload(name: str, args, world: int, rank: int, local: int) -> dict
         "cpu_baseline": cpu_baseline,
     }
     op.close()
-    del dev, pk, pv, out, ws, flush, flush_words, call, opt
+    del dev, pk, pv, out, ws, flush, flush_words, call, opt, call_e2e, staged, dev_stage, host_stage
     torch.cuda.empty_cache()
     return rec
 
