@@ -854,50 +854,57 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
               if (hf == 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.o_done[q], (uint32_t)(t - 1) & 1u, p.wait_budget)))
                 half_ok = false;
               tc_fence_after();
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(o_addr + c * 32, raw);
+#pragma unroll 1
+              for (int c = 0; c < 8; ++c) {   // 16 columns at a time (the half's scores stay live)
+                uint32_t raw[16];
+                tmem_ld16(o_addr + c * 16, raw);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
-                tmem_st32(o_addr + c * 32, raw);
+                for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+                tmem_st16(o_addr + c * 16, raw);
               }
             }
             if (hf == 1) {
               // P of the first half was written with the old reference.
-              uint32_t pk[32];
               tmem_st_wait();
-              tmem_ld32(s_a, pk);
-              tmem_ld_wait();
               const float2 f2 = make_float2(f, f);
+#pragma unroll 1
+              for (int c = 0; c < 2; ++c) {
+                uint32_t pk[16];
+                tmem_ld16(s_a + c * 16, pk);
+                tmem_ld_wait();
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
-                const float2 w = ffma2(v, f2, make_float2(0.f, 0.f));
-                const __half2 hw = __floats2half2_rn(w.x, w.y);
-                pk[k] = *reinterpret_cast<const uint32_t*>(&hw);
+                for (int k = 0; k < 16; ++k) {
+                  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&pk[k]));
+                  const float2 w = ffma2(v, f2, make_float2(0.f, 0.f));
+                  const __half2 hw = __floats2half2_rn(w.x, w.y);
+                  pk[k] = *reinterpret_cast<const uint32_t*>(&hw);
+                }
+                tmem_st16(s_a + c * 16, pk);
               }
-              tmem_st32(s_a, pk);
             }
             l_run *= f;
             ls2.x *= f;
             ls2.y *= f;
             m_run = m_new;
           }
-          // Masked scores are -inf: exp2 gives 0.
+          // Masked scores are -inf: exp2 gives 0. P goes out 16 columns at a time.
           const float2 negm2 = make_float2(-m_run, -m_run);
-          uint32_t packed[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float2 arg = ffma2(make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])),
-                                     make_float2(1.f, 1.f), negm2);
-            const float pa = ex2(arg.x), pb = ex2(arg.y);
-            ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
-            const __half2 hp = __floats2half2_rn(pa, pb);
-            packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int e = 32 * h2 + 2 * k;
+              const float2 arg = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                       make_float2(1.f, 1.f), negm2);
+              const float pa = ex2(arg.x), pb = ex2(arg.y);
+              ls2 = ffma2(make_float2(pa, pb), make_float2(1.f, 1.f), ls2);
+              const __half2 hp = __floats2half2_rn(pa, pb);
+              packed[k] = *reinterpret_cast<const uint32_t*>(&hp);
+            }
+            tmem_st16(s_a + hf * 32 + 16 * h2, packed);
           }
-          tmem_st32(s_a + hf * 32, packed);
         }
         if (!half_ok) {
           ok = false;
