@@ -187,6 +187,15 @@ PREFILL = {
                                                 capacity=700, seqlens_k=(699, 400), seqlens_range=None,
                                                 quant="PER_CHANNEL", bits=4, qk_norm=True, rotary_theta=1e4,
                                                 local_window_size=300, scale_range=(0.15, 0.4)),
+    # group sizes 16 and 128: a query tile holds 8 and 1 positions (4-D copy boxes of 16 and 128 heads)
+    "i8_tcq_g16_causal_norm_rotary": spec(dtype="f32", B=2, S=40, N=32, Nkv=2, capacity=700, seqlens_range=(40, 690),
+                                          quant="PER_CHANNEL", qk_norm=True, rotary_theta=1e4,
+                                          scale_range=(0.01, 0.05)),
+    "i4_tcq_g128_prompt": spec(dtype="f32", B=2, S=20, N=128, Nkv=1, mode="prompt", capacity=24,
+                               seqlens_k=(19, 7), seqlens_range=None, quant="PER_TENSOR", bits=4,
+                               scale_range=(0.2, 0.3)),
+    "i8_g3_simt_fallback": spec(dtype="f32", S=20, N=6, Nkv=2, quant="PER_CHANNEL", seqlens_range=(20, 500),
+                                scale_range=(0.01, 0.05)),
     "i4_h256_window_generic_prepass": spec(dtype="f32", H=256, N=4, Nkv=2, S=20, mode="prompt", capacity=24,
                                            seqlens_k=(19, 19, 10), seqlens_range=None, quant="PER_CHANNEL", bits=4,
                                            local_window_size=5, scale_range=(0.1, 0.3)),
