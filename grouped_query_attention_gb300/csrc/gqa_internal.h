@@ -118,6 +118,18 @@ __host__ __device__ inline BatchRows batch_rows(const Params& p, int total, int 
   return r;
 }
 
+// Launch order of the flash prefills, whose CTAs are (query block of 256
+// rows, KV head (b, g)) pairs. Without a past cache (prompt) a block's key
+// range depends only on its query block, and a grid that runs
+// query-block-major (x = KV head, y = query block from the last) starts the
+// longest blocks of every KV head first and leaves the short ones for the
+// tail. With a past the lengths also depend on seqlens_k (device data): the
+// grid runs KV-head-major (x = query block from the last, y = KV head),
+// longest first within a head. Each kernel states when it takes the first.
+__host__ __device__ inline bool prefill_prompt_qb_major(const Params& p) {
+  return p.mode == kPrompt && (p.S * p.G + 255) / 256 <= 65535;
+}
+
 // Size of the fixed scratch array behind gqa_forward_noalloc (16 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 // Device address of that array on the current device (looked up once per device).

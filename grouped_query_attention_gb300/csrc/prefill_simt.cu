@@ -34,6 +34,15 @@ constexpr int kK = 64;          // keys per tile
 constexpr int kKP = kK + 4;     // padded K^T row (keeps 16-byte alignment)
 constexpr int kMaxH = 256;
 
+// Launch order: prompt calls (no past: a block's key range depends only on
+// its row block) run row-block-major over all KV heads, so the longest blocks
+// of every head start first; otherwise one grid row per KV head, its longest
+// blocks first. (Row blocks in rising order, shortest first, took 427-431
+// against 342 us on a causal fp32 B=2, S=1024, 16-head prompt.)
+__host__ __device__ inline bool simt_rb_major(const Params& p) {
+  return p.mode == kPrompt && (p.S * p.G + kR - 1) / kR <= 65535;
+}
+
 template <int HMAX>
 constexpr size_t smem_floats() {
   return (size_t)HMAX * kR + (size_t)HMAX * kKP + (size_t)kK * HMAX + (size_t)kR * kKP;
@@ -79,7 +88,13 @@ prefill_simt_kernel(const Params p) {
 
   const int H = p.H;
   const int tid = threadIdx.x, rg = tid >> 4, kg = tid & 15;
-  const int rb = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // Row blocks from the last (longest key ranges first), in the order of
+  // simt_rb_major.
+  const int nrb = (p.S * p.G + kR - 1) / kR;
+  const bool rbm = simt_rb_major(p);
+  const int rb = nrb - 1 - (int)(rbm ? blockIdx.y : blockIdx.x);
+  const int g = rbm ? (int)(blockIdx.x % p.Nkv) : (int)blockIdx.y;
+  const int b = rbm ? (int)(blockIdx.x / p.Nkv) : (int)blockIdx.z;
   const int total = p.seqlens[b] + 1;
   const int past = batch_past(p, total);
   if (past < 0) {
@@ -317,8 +332,8 @@ cudaError_t launch_h(const Params& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     set[dev] = true;
   }
-  const int nrows = p.S * p.G;
-  dim3 grid((nrows + kR - 1) / kR, p.Nkv, p.B), block(kThreads);
+  const unsigned nrb = (unsigned)((p.S * p.G + kR - 1) / kR);
+  const dim3 grid = simt_rb_major(p) ? dim3((unsigned)(p.B * p.Nkv), nrb) : dim3(nrb, p.Nkv, p.B), block(kThreads);
   prefill_simt_kernel<T, CacheT, HMAX><<<grid, block, smem, st>>>(p);
   return cudaGetLastError();
 }

@@ -176,6 +176,14 @@ __device__ __forceinline__ void load_bias32(const __half* row, int j, int col0, 
   }
 }
 
+// Query-block-major launch (prefill_prompt_qb_major) for prompts without a
+// causal mask, where every block of a call is equally long: measured faster
+// (202.7 against 208.9 us on a bidirectional B=4, S=2048 prompt). Causal
+// prompts keep the KV-head-major order, in which the 64 blocks of a head run
+// together over its K/V tiles (query-block-major measured 451 against 448 us
+// on the causal B=4, S=4096 prompt).
+__host__ __device__ inline bool tc_qb_major(const Params& p) { return prefill_prompt_qb_major(p) && !p.causal; }
+
 __device__ __forceinline__ bool aborted(const TcSmem& sm) {
   return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
 }
@@ -323,8 +331,9 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nrows = p.S * p.G;
   const int nqb = (nrows + 2 * kBM - 1) / (2 * kBM);
-  const int qb = nqb - 1 - (int)blockIdx.x;  // longest key ranges first
-  const int bg = blockIdx.y, b = bg / p.Nkv, g = bg % p.Nkv;
+  const bool qbm = tc_qb_major(p);
+  const int qb = nqb - 1 - (int)(qbm ? blockIdx.y : blockIdx.x);  // longest key ranges first
+  const int bg = (int)(qbm ? blockIdx.x : blockIdx.y), b = bg / p.Nkv, g = bg % p.Nkv;
 
   // ---- block-uniform checks before any barrier or tensor memory
   const int total = p.seqlens[b] + 1;
@@ -1060,7 +1069,8 @@ cudaError_t launch_prefill_tc(const Params& p, cudaStream_t st, const TmaMaps& m
     g_smem_set[variant][dev] = true;
   }
   const int nrows = p.S * p.G;
-  dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
+  const unsigned nqb = (unsigned)((nrows + 2 * kBM - 1) / (2 * kBM)), nbg = (unsigned)(p.B * p.Nkv);
+  const dim3 grid = tc_qb_major(p) ? dim3(nbg, nqb) : dim3(nqb, nbg);
   kern<<<grid, threads_for(mode), smem, st>>>(p, maps.m[0], maps.m[1], maps.m[2], maps.m[3], maps.m[4]);
   return cudaGetLastError();
 }

@@ -320,8 +320,11 @@ prefill_tcq_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nrows = p.S * p.G;
   const int nqb = (nrows + 2 * kBM - 1) / (2 * kBM);
-  const int qb = nqb - 1 - (int)blockIdx.x;  // longest key ranges first
-  const int bg = blockIdx.y, b = bg / p.Nkv, g = bg % p.Nkv;
+  // Query-block-major for prompts (127 against 145 us on the causal int8
+  // B=2, S=2048 prompt: with three to four waves of CTAs the tail counts).
+  const bool qbm = prefill_prompt_qb_major(p);
+  const int qb = nqb - 1 - (int)(qbm ? blockIdx.y : blockIdx.x);  // longest key ranges first
+  const int bg = (int)(qbm ? blockIdx.x : blockIdx.y), b = bg / p.Nkv, g = bg % p.Nkv;
 
   // ---- block-uniform checks before any barrier or tensor memory
   const int total = p.seqlens[b] + 1;
@@ -759,7 +762,8 @@ cudaError_t launch_prefill_tcq(const Params& p, cudaStream_t st, const TmaMaps& 
     g_smem_set[variant][dev] = true;
   }
   const int nrows = p.S * p.G;
-  dim3 grid((nrows + 2 * kBM - 1) / (2 * kBM), p.B * p.Nkv);
+  const unsigned nqb = (unsigned)((nrows + 2 * kBM - 1) / (2 * kBM)), nbg = (unsigned)(p.B * p.Nkv);
+  const dim3 grid = prefill_prompt_qb_major(p) ? dim3(nbg, nqb) : dim3(nqb, nbg);
   kern<<<grid, kThreads, smem, st>>>(p, maps.m[0], maps.m[1]);
   return cudaGetLastError();
 }
