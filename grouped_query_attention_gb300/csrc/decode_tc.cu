@@ -212,12 +212,11 @@ __device__ __forceinline__ int batch_tiles(const Params& p, int b, int& past, in
 }
 
 // Work units of a (b, g) with `tiles` tiles: one per tile plus kEndUnits for
-// the end of its key range (the epilogue that writes the output or a partial).
-// Shares are equal in units, so a CTA that ends more key ranges gets fewer
-// tiles. Measured over weights 0 to 12 on the fp16 (B=16, C=8192) and int8
-// (B=32, C=16384) decodes: 2 is fastest (fp16 55.3 us against 56.1 with 5,
-// 57.1 with 0 or 8).
-constexpr int kEndUnits = 2;
+// the end of its key range (the epilogue that writes the output or a partial
+// costs about as much as that many tiles). Shares are equal in units, so a
+// CTA that ends more key ranges gets fewer tiles. (A weight of 2 measured
+// 56.4-56.6 us against 54.4-55.4 with 5 on the fp16 B=16, C=8192 decode.)
+constexpr int kEndUnits = 5;
 __device__ __forceinline__ long long bg_units(int tiles) { return tiles > 0 ? tiles + kEndUnits : 0; }
 
 // Number of work units over all (b, g) (whole warp).
