@@ -355,3 +355,41 @@ def test_set_wait_limit_argument_checks():
         assert lib.gqa_set_wait_limit(h, 0, -1) == capi.GQA_OK
     finally:
         capi.gqa_destroy(h)
+
+
+def test_call_reuses_descriptors_while_tensors_stay(monkeypatch):
+    """The binding rebuilds the C descriptors (and asks the workspace size again) only when a
+    tensor's address, shape, dtype or layout, the total length or the set of inputs changes;
+    every call passes the descriptors of the tensors it was given."""
+    import torch
+
+    import grouped_query_attention_gb300 as G
+
+    sizes, seen = [], []
+    monkeypatch.setattr(capi, "gqa_workspace_size", lambda h, i, o: sizes.append(1) or 256)
+    monkeypatch.setattr(capi, "gqa_forward", lambda h, i, o, ws, n, st: seen.append(
+        (i.query.data, i.query.shape[2], i.cos_cache.data, o.output.data, i.total_sequence_length)))
+    op = G.GroupQueryAttention(num_heads=4, kv_num_heads=2)
+    base = torch.zeros(256)
+    q = base[:128].view(1, 1, 128)
+    k, v = torch.zeros(1, 1, 64), torch.zeros(1, 1, 64)
+    pk, pv = torch.zeros(1, 2, 8, 32), torch.zeros(1, 2, 8, 32)
+    call = dict(query=q, key=k, value=v, seqlens_k=torch.zeros(1, dtype=torch.int32), total_sequence_length=1,
+                present_key=pk, present_value=pv, output=torch.empty(1, 1, 128), past_key=pk, past_value=pv,
+                workspace=torch.empty(256, dtype=torch.uint8), stream=0)
+    op(**call)
+    op(**call)
+    assert len(sizes) == 1 and len(seen) == 2 and seen[0] == seen[1]
+    q2 = torch.zeros(1, 1, 128)
+    op(**dict(call, query=q2))                                  # another address
+    assert len(sizes) == 2 and seen[-1][0] == q2.data_ptr()
+    op(**dict(call, total_sequence_length=2))                   # another total length
+    assert len(sizes) == 3 and seen[-1][4] == 2
+    cos = torch.zeros(8, 16)
+    op(**dict(call, cos_cache=cos, sin_cache=cos))              # another set of inputs
+    assert len(sizes) == 4 and seen[-1][2] == cos.data_ptr()
+    op(**call)
+    assert len(sizes) == 5 and seen[-1] == seen[0]
+    strided = base.as_strided((1, 1, 128), (256, 256, 2))      # same address, shape and dtype, not contiguous
+    with pytest.raises(ValueError):
+        op(**dict(call, query=strided))
