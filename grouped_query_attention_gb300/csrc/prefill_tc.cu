@@ -184,6 +184,14 @@ __device__ __forceinline__ void load_bias32(const __half* row, int j, int col0, 
 // on the causal B=4, S=4096 prompt).
 __host__ __device__ inline bool tc_qb_major(const Params& p) { return prefill_prompt_qb_major(p) && !p.causal; }
 
+// Causal prompts run KV-head-major, but the nqb / 8 shortest query blocks of
+// every head are held back to the end of the grid, so that short blocks and
+// not a late head's longest ones fill the tail while the long blocks keep
+// starting at staggered times.
+__host__ __device__ inline int tc_short_blocks(const Params& p, int nqb) {
+  return p.mode == kPrompt && p.causal ? nqb / 8 : 0;
+}
+
 __device__ __forceinline__ bool aborted(const TcSmem& sm) {
   return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
 }
@@ -331,9 +339,23 @@ prefill_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nrows = p.S * p.G;
   const int nqb = (nrows + 2 * kBM - 1) / (2 * kBM);
-  const bool qbm = tc_qb_major(p);
-  const int qb = nqb - 1 - (int)(qbm ? blockIdx.y : blockIdx.x);  // longest key ranges first
-  const int bg = (int)(qbm ? blockIdx.x : blockIdx.y), b = bg / p.Nkv, g = bg % p.Nkv;
+  int qb, bg;   // longest key ranges first
+  if (tc_qb_major(p)) {
+    qb = nqb - 1 - (int)blockIdx.y;
+    bg = (int)blockIdx.x;
+  } else {
+    // KV-head-major; the ks shortest query blocks of every head follow all the others.
+    const int ks = tc_short_blocks(p, nqb);
+    const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x), n1 = (int)gridDim.y * (nqb - ks);
+    if (lin < n1) {
+      bg = lin / (nqb - ks);
+      qb = nqb - 1 - lin % (nqb - ks);
+    } else {
+      bg = (lin - n1) / ks;
+      qb = ks - 1 - (lin - n1) % ks;
+    }
+  }
+  const int b = bg / p.Nkv, g = bg % p.Nkv;
 
   // ---- block-uniform checks before any barrier or tensor memory
   const int total = p.seqlens[b] + 1;
